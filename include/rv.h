@@ -1,0 +1,166 @@
+/*
+ * rv.h - C ABI of the River-LLM token-level early-exit decode library
+ * (librv.so, CUDA, sm_103a).
+ *
+ * The method: "River-LLM: Large Language Model Seamless Exit Based on KV
+ * Share" (Shen, Zou).  Page summaries used as the definition:
+ *   - paperlayer.ai summary, section 4 "KV-Shared Exit Layer": every exit
+ *     layer is a plug-in copy of the backbone layer with the same index,
+ *     4-bit weight-only quantized, addressing the backbone's KV cache.
+ *   - same page, section 4 "Inference with Seamless Exit": exit layers run
+ *     in series from a predefined entry layer; after an exit the remaining
+ *     layers run as exit layers and the original LM head gives the logits;
+ *     prefill uses one sequence-level exit, generation a token-level exit.
+ *   - aitrends.kr article: s(l) = cos(h(l-1), h(l)) between the input and
+ *     output of layer l; a token exits when s(l) is greater than tau; the
+ *     exit layers are W4A16 copies of the backbone blocks.
+ *
+ * Conventions
+ *   - Every call returns an int status (RV_OK or a negative RV_E* code) and
+ *     records a message readable with rv_last_error() on the calling thread.
+ *     No call throws, aborts the process or traps on the device.
+ *   - The library owns all device memory behind the opaque rv_model handle:
+ *     backbone weights, river copies, the KV cache, activations, scratch.
+ *   - The caller owns every array passed in.  Pointers are HOST pointers
+ *     unless the function name ends in _dev, in which case they are DEVICE
+ *     pointers on the model's device and the call is asynchronous on the
+ *     model's stream.
+ *   - Layers are numbered 1..L.  An exit layer e in 1..L means layers 1..e
+ *     ran in the backbone and e+1..L in the river; e = L means the token never
+ *     left the backbone; e = 0 (forced mode only) means every layer ran in the
+ *     river.
+ *   - 16-bit types: act_dtype 0 = fp16, 1 = bf16.  Weights, the KV cache and
+ *     every activation that enters a matrix product use it; the residual
+ *     stream, accumulations, norms, softmax and s(l) are fp32.
+ */
+#ifndef RV_H
+#define RV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RV_OK 0
+#define RV_EINVAL (-1)     /* bad argument (range, pointer, shape) */
+#define RV_ENOMEM (-2)     /* device or pinned host allocation failed; nothing leaked */
+#define RV_ECUDA (-3)      /* a CUDA runtime call failed */
+#define RV_ECAPACITY (-4)  /* a row's KV cache is full (len == max_seq); nothing changed */
+#define RV_ESTATE (-5)     /* call out of order, e.g. tau-rule decode before rv_quantize_river */
+#define RV_ETIMEOUT (-6)   /* reserved: a bounded device wait gave up */
+
+/* Projection ids of a decoder layer (for rv_export_river). */
+#define RV_PROJ_Q 0
+#define RV_PROJ_K 1
+#define RV_PROJ_V 2
+#define RV_PROJ_O 3
+#define RV_PROJ_GATE 4
+#define RV_PROJ_UP 5
+#define RV_PROJ_DOWN 6
+
+/* What rv_debug_dump copies out (all host layouts, row-major). */
+#define RV_DUMP_HIDDEN 0  /* float [L+1][B][d]: residual stream after layers 0..L of the last step */
+#define RV_DUMP_S 1       /* float [L][B]: s(l) of the last step, NaN where not evaluated */
+#define RV_DUMP_LOGITS 2  /* float [B][V]: logits of the last step */
+#define RV_DUMP_KV 3      /* uint16 [L][2][max_batch][Hkv][max_seq][hd]: the whole cache */
+#define RV_DUMP_LENS 4    /* int32 [max_batch]: cached positions per row */
+
+typedef struct rv_model rv_model; /* opaque */
+
+/* Decoder shape (Llama-style: RMSNorm, GQA with rotate-half RoPE, SwiGLU).
+ * max_batch and max_seq size the KV cache once, at load. */
+typedef struct rv_config {
+  int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  int tied_embed; /* 1: the LM head is the embedding matrix */
+  int act_dtype;  /* 0 = fp16, 1 = bf16 */
+  float rms_eps, rope_theta;
+  int max_batch, max_seq;
+} rv_config;
+
+/* Last error message of the calling thread ("" if none). */
+const char *rv_last_error(void);
+
+/* Load a backbone.  weights holds 3 + 9*L host pointers to 16-bit arrays in
+ * this order: embedding [V][d], final norm [d], LM head [V][d] (NULL when
+ * tied_embed), then per layer: attention norm [d], W_q [H*hd][d],
+ * W_k [Hkv*hd][d], W_v [Hkv*hd][d], W_o [d][H*hd], MLP norm [d],
+ * W_gate [F][d], W_up [F][d], W_down [d][F].  The arrays are copied to the
+ * device; the caller may free them afterwards.  stream is a cudaStream_t
+ * (NULL: the library creates its own).  Allocates the one KV cache for
+ * max_batch x max_seq positions, filled with the sentinel 0x7FFF (a NaN in
+ * both 16-bit types).  Requires d_model, ffn and H*hd multiples of 8 and
+ * head_dim in {64, 128}.  On failure nothing stays allocated. */
+int rv_load_model(const rv_config *cfg, const void *const *weights, void *stream, rv_model **out);
+
+/* Build the river: for every layer, copy the 7 projection matrices and
+ * quantize them to int4 by round-to-nearest, asymmetric, per output row and
+ * per group of group_size consecutive input columns, with an fp16 scale and
+ * an fp16 (integer-valued) zero point; the exit layers share the backbone's
+ * RMSNorm gains, RoPE and KV cache and allocate no KV memory.
+ * entry_layer (1..L) is the first layer after which a token may exit by the
+ * tau rule.  group_size: a multiple of 32.  Returns RV_EINVAL if a group's
+ * scale overflows fp16.  May be called again (rebuilds the river). */
+int rv_quantize_river(rv_model *m, int group_size, int entry_layer);
+
+/* Copy one river matrix out in the canonical layout: q as uint32
+ * [N][K/8] with element k of a row in bits 4*(k%8).. of word k/8, scales and
+ * zeros as fp16 [N][ceil(K/group)].  layer in 1..L, proj an RV_PROJ_* id.
+ * Any of the three pointers may be NULL. */
+int rv_export_river(const rv_model *m, int layer, int proj, void *q_packed, void *scales, void *zeros);
+
+/* Prefill rows 0..B-1 with tokens [B][T0] (row-major int32), starting each
+ * row over at position 0, and return the first generated id per row.
+ * Sequence-level exit: with fixed_exit_layer = -1 a row's exit layer is the
+ * first l in [entry, L-1] at which s_t(l) > tau for every prompt token t
+ * (else L); with fixed_exit_layer in 0..L it is that layer.  exit_layer[b]
+ * receives it.  Cache slots at positions >= T0 keep their contents (use
+ * rv_kv_reset first to restore the sentinel). */
+int rv_prefill(rv_model *m, const int32_t *tokens, int B, int T0, float tau, int fixed_exit_layer,
+               int32_t *next_ids, int32_t *exit_layer);
+
+/* One decode step for rows 0..B-1: token b enters at position len_b, every
+ * layer 1..L writes its K and V into slot (l, b, len_b) whichever path the
+ * row takes, then len_b += 1.  Token-level exit: a row leaves the backbone
+ * after the first layer l in [entry, L-1] with s(l) > tau and finishes in the
+ * river.  forced_exit (NULL for the tau rule) gives each row's exit layer
+ * 0..L instead.  next_ids[b] is the greedy id (lowest index on ties),
+ * exit_layer[b] the row's exit layer.  RV_ECAPACITY if any row has
+ * len_b == max_seq (nothing is changed). */
+int rv_decode_step(rv_model *m, const int32_t *tokens, int B, float tau, const int32_t *forced_exit,
+                   int32_t *next_ids, int32_t *exit_layer);
+
+/* rv_decode_step with device pointers, asynchronous on the model's stream.
+ * Arguments are checked on the host except token values and forced exit
+ * values, which the device checks: an out-of-range value sets a device error
+ * flag (reported by rv_sync_status) and is treated as token 0 / exit L. */
+int rv_decode_step_dev(rv_model *m, const int32_t *d_tokens, int B, float tau, const int32_t *d_forced_exit,
+                       int32_t *d_next_ids, int32_t *d_exit_layer);
+
+/* Wait for the model's stream and report any device-side error flag. */
+int rv_sync_status(rv_model *m);
+
+/* Forget the cached positions of the given rows (NULL: all rows) and refill
+ * their cache slots with the sentinel. */
+int rv_kv_reset(rv_model *m, const int32_t *rows, int n_rows);
+
+/* Keep per-step debug copies (hidden states per layer, s(l), logits) when
+ * enable != 0.  Costs extra device writes; off by default. */
+int rv_set_debug(rv_model *m, int enable);
+
+/* Copy a debug buffer or the cache out (see RV_DUMP_*).  bytes must equal
+ * the buffer's size for max_batch rows (hidden, s, logits use B = max_batch). */
+int rv_debug_dump(rv_model *m, int what, void *dst, size_t bytes);
+
+/* Sizes, for callers that allocate dump buffers. */
+size_t rv_kv_bytes(const rv_model *m);
+size_t rv_param_bytes(const rv_model *m, int which /* 0 backbone, 1 river */);
+
+/* Free everything the model owns. */
+void rv_free_model(rv_model *m);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,862 @@
+// Host runtime of librv: the C ABI declared in include/rv.h.
+//
+// Owns the device copy of the backbone, the river copies, the one shared KV
+// cache and all activations; runs prefill (sequence-level exit) and decode
+// steps (token-level exit) on the model's stream.  Decode steps are captured
+// once per batch size in a CUDA graph: every per-step value (tokens, tau,
+// forced exits, positions, routes) lives in device memory, so a step is one
+// host-to-device copy, one graph launch and one device-to-host copy.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <map>
+#include <string>
+#include <vector>
+
+#include "../../include/rv.h"
+#include "common.cuh"
+#include "kernels.cuh"
+
+using namespace rv;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define RV_CK(call)                                                                               \
+  do {                                                                                            \
+    cudaError_t e_ = (call);                                                                      \
+    if (e_ != cudaSuccess) {                                                                      \
+      return fail(e_ == cudaErrorMemoryAllocation ? RV_ENOMEM : RV_ECUDA, "%s failed: %s", #call, \
+                  cudaGetErrorString(e_));                                                        \
+    }                                                                                             \
+  } while (0)
+
+constexpr uint16_t KV_SENTINEL = 0x7FFF;
+enum { MAT_QKV = 0, MAT_O = 1, MAT_GU = 2, MAT_D = 3, N_MAT = 4 };
+
+struct RiverDev {
+  uint32_t *q = nullptr;
+  __half *s = nullptr, *z = nullptr;
+  int Kp = 0, G = 0;
+};
+
+struct LayerDev {
+  uint16_t *attn_norm = nullptr, *mlp_norm = nullptr;
+  uint16_t *w[N_MAT] = {nullptr, nullptr, nullptr, nullptr};
+  RiverDev r[N_MAT];
+};
+
+inline int round32(int k) { return (k + 31) & ~31; }
+
+}  // namespace
+
+struct rv_model {
+  rv_config c{};
+  int act = 1, L = 0, d = 0, H = 0, Hkv = 0, hd = 0, F = 0, V = 0, Bmax = 0, Tmax = 0;
+  int qd = 0, kvd = 0, qkv_n = 0;
+  int dev = 0, n_sm = 0;
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+
+  std::vector<void *> allocs;  // every device allocation (freed at rv_free_model)
+  void *pinned = nullptr;
+
+  uint16_t *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
+  std::vector<LayerDev> layers;
+  int group = 0, entry = 1;
+  bool has_river = false;
+  std::vector<void *> river_allocs;
+
+  KVGeom kv{};
+  size_t kv_bytes = 0;
+  float2 *rope_cs = nullptr;
+
+  // device state block (int32 words), see state_layout()
+  int32_t *d_state = nullptr;
+  int in_words = 0, out_words = 0;
+  StepState st{};
+  int32_t *d_counts = nullptr, *d_nrows = nullptr, *d_ident = nullptr;
+  std::vector<int32_t> h_len;
+
+  // batch-1 activations
+  float *hbuf[2] = {nullptr, nullptr}, *hmid = nullptr, *qbuf = nullptr, *obuf = nullptr, *abuf = nullptr;
+  float *partials = nullptr;
+  unsigned *counters = nullptr;
+  int attn_splits_b1 = 1, attn_splits_max = 1;
+  float *attn_part = nullptr;
+  unsigned *attn_counter = nullptr;
+
+  // general-path workspace (grown on demand)
+  long ws_rows = 0;
+  std::vector<void *> ws_allocs;
+  float *gH = nullptr, *gHin = nullptr, *gX = nullptr, *gY = nullptr, *gY2 = nullptr, *gQ = nullptr, *gO = nullptr;
+  int32_t *gLists = nullptr, *gTokens = nullptr;
+  float *gHf = nullptr, *gXf = nullptr, *gLogits = nullptr;
+
+  // debug copies
+  bool debug = false;
+  float *dbg_h = nullptr, *dbg_s = nullptr, *dbg_logits = nullptr;
+
+  // graphs
+  std::map<int, cudaGraphExec_t> graphs;
+};
+
+namespace {
+
+int dalloc(rv_model *m, std::vector<void *> &list, void **p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return fail(RV_ENOMEM, "cudaMalloc(%zu bytes) failed: %s", bytes, cudaGetErrorString(e));
+  }
+  list.push_back(*p);
+  return RV_OK;
+}
+
+#define RV_ALLOC(list, ptr, bytes)                                              \
+  do {                                                                          \
+    int rc_ = dalloc(m, list, reinterpret_cast<void **>(&(ptr)), (bytes));      \
+    if (rc_ != RV_OK) return rc_;                                               \
+  } while (0)
+
+void free_list(std::vector<void *> &list) {
+  for (void *p : list) cudaFree(p);
+  list.clear();
+}
+
+void drop_graphs(rv_model *m) {
+  for (auto &kv : m->graphs) cudaGraphExecDestroy(kv.second);
+  m->graphs.clear();
+}
+
+// int32 state block: [in: tokens B | forced B | mode | tau | entry | nrows]
+//                    [out: next B | exit B | err | pad] [route B | len B | counts 2 | pad 2]
+void state_layout(rv_model *m) {
+  const int B = m->Bmax;
+  m->in_words = 2 * B + 4;
+  m->out_words = 2 * B + 2;
+  int32_t *s = m->d_state;
+  StepState &st = m->st;
+  st.tokens = s;
+  st.forced = s + B;
+  st.mode = s + 2 * B;
+  st.tau = reinterpret_cast<const float *>(s + 2 * B + 1);
+  st.entry = s + 2 * B + 2;
+  m->d_nrows = s + 2 * B + 3;
+  int32_t *o = s + m->in_words;
+  st.next_ids = o;
+  st.exit_layer = o + B;
+  st.err = o + 2 * B;
+  int32_t *r = o + m->out_words;
+  st.route = r;
+  st.len = r + B;
+  m->d_counts = r + 2 * B;
+}
+
+size_t state_words(int B) { return (size_t)(2 * B + 4) + (2 * B + 2) + (2 * B + 4); }
+
+int32_t *pin_in(rv_model *m) { return static_cast<int32_t *>(m->pinned); }
+int32_t *pin_out(rv_model *m) { return static_cast<int32_t *>(m->pinned) + m->in_words; }
+
+Mat make_mat(const rv_model *m, const LayerDev &ly, int which) {
+  Mat mt{};
+  mt.w = ly.w[which];
+  switch (which) {
+    case MAT_QKV: mt.N = m->qkv_n; mt.K = m->d; break;
+    case MAT_O: mt.N = m->d; mt.K = m->qd; break;
+    case MAT_GU: mt.N = 2 * m->F; mt.K = m->d; break;
+    default: mt.N = m->d; mt.K = m->F; break;
+  }
+  if (m->has_river) {
+    mt.r.q = ly.r[which].q;
+    mt.r.s = ly.r[which].s;
+    mt.r.z = ly.r[which].z;
+    mt.r.Kp = ly.r[which].Kp;
+    mt.r.G = ly.r[which].G;
+    mt.r.g = m->group;
+  }
+  return mt;
+}
+
+int gemv_grid(const rv_model *m, int units) {
+  int g = (units + 7) / 8;
+  const int cap = 4 * m->n_sm;
+  return g < cap ? g : cap;
+}
+
+// -------------------------------------------------------------- batch-1 step
+
+int enqueue_step_b1(rv_model *m, cudaStream_t s) {
+  const int L = m->L, B = m->Bmax;
+  RV_CK(cudaMemsetAsync(m->st.err, 0, sizeof(int32_t), s));
+  RV_CK(launch_step_init(m->st, 1, L, s));
+  RV_CK(launch_embed(m->embed, m->d, m->act, m->st.tokens, 1, m->V, m->hbuf[0], m->debug ? m->dbg_h : nullptr,
+                     m->st.err, s));
+  for (int l = 0; l < L; ++l) {
+    const LayerDev &ly = m->layers[l];
+    float *hin = m->hbuf[l & 1], *hout = m->hbuf[(l + 1) & 1];
+    GemvArgs a{};
+    a.st = m->st;
+    a.kv = m->kv;
+    a.layer = l;
+    a.L = L; a.H = m->H; a.Hkv = m->Hkv; a.hd = m->hd;
+    a.eps = m->c.rms_eps;
+    a.rope_cs = m->rope_cs;
+    a.partials = m->partials;
+
+    // attention in: RMSNorm -> QKV -> RoPE -> K/V append
+    a.m = make_mat(m, ly, MAT_QKV);
+    a.units = m->qkv_n / 2;
+    a.h = hin; a.gamma = ly.attn_norm; a.out_vec = m->qbuf;
+    RV_CK(launch_gemv_b1(m->act, PRO_NORM, EPI_QKV, a, gemv_grid(m, a.units), s));
+
+    AttnArgs at{};
+    at.kv = m->kv; at.layer = l; at.H = m->H; at.Hkv = m->Hkv; at.hd = m->hd; at.act = m->act;
+    at.q = m->qbuf; at.o = m->obuf; at.len = m->st.len; at.splits = m->attn_splits_b1;
+    at.part = m->attn_part; at.counter = m->attn_counter;
+    RV_CK(launch_attn_decode(at, 1, s));
+
+    // O projection + residual
+    a.m = make_mat(m, ly, MAT_O);
+    a.units = m->d;
+    a.vec = m->obuf; a.h_base = hin; a.h_out = m->hmid;
+    RV_CK(launch_gemv_b1(m->act, PRO_VEC, EPI_RESID, a, gemv_grid(m, a.units), s));
+
+    // MLP in: RMSNorm -> gate/up -> SwiGLU
+    a.m = make_mat(m, ly, MAT_GU);
+    a.units = m->F;
+    a.h = m->hmid; a.gamma = ly.mlp_norm; a.out_vec = m->abuf;
+    RV_CK(launch_gemv_b1(m->act, PRO_NORM, EPI_SWIGLU, a, gemv_grid(m, a.units), s));
+
+    // down projection + residual + s(l) + exit decision
+    a.m = make_mat(m, ly, MAT_D);
+    a.units = m->d;
+    a.vec = m->abuf; a.h_base = m->hmid; a.h_in = hin; a.h_out = hout;
+    a.counter = m->counters + l;
+    a.dbg_h = m->debug ? m->dbg_h + (size_t)(l + 1) * B * m->d : nullptr;
+    a.dbg_s = m->debug ? m->dbg_s + (size_t)l * B : nullptr;
+    RV_CK(launch_gemv_b1(m->act, PRO_VEC, EPI_DOWN, a, gemv_grid(m, a.units), s));
+  }
+  // final RMSNorm + LM head + greedy argmax
+  GemvArgs a{};
+  a.st = m->st;
+  a.m.w = m->lm_head; a.m.N = m->V; a.m.K = m->d;
+  a.units = m->V;
+  a.h = m->hbuf[L & 1]; a.gamma = m->final_norm; a.eps = m->c.rms_eps;
+  a.partials = m->partials;
+  a.counter = m->counters + L;
+  a.dbg_logits = m->debug ? m->dbg_logits : nullptr;
+  RV_CK(launch_gemv_b1(m->act, PRO_NORM, EPI_LOGITS, a, gemv_grid(m, a.units), s));
+  return RV_OK;
+}
+
+// -------------------------------------------------------------- general path
+
+int ensure_ws(rv_model *m, long rows) {
+  if (rows <= m->ws_rows) return RV_OK;
+  // captured graphs hold workspace pointers: drop them before reallocating
+  RV_CK(cudaStreamSynchronize(m->stream));
+  drop_graphs(m);
+  free_list(m->ws_allocs);
+  m->ws_rows = 0;
+  const size_t d = m->d, F = m->F, qd = m->qd;
+  size_t xw = d > F ? d : F;
+  if (qd > xw) xw = qd;
+  size_t yw = (size_t)m->qkv_n;
+  if (2 * F > yw) yw = 2 * F;
+  if (d > yw) yw = d;
+  auto &L = m->ws_allocs;
+  RV_ALLOC(L, m->gH, sizeof(float) * rows * d);
+  RV_ALLOC(L, m->gHin, sizeof(float) * rows * d);
+  RV_ALLOC(L, m->gX, sizeof(float) * rows * xw);
+  RV_ALLOC(L, m->gY, sizeof(float) * rows * yw);
+  RV_ALLOC(L, m->gY2, sizeof(float) * rows * d);
+  RV_ALLOC(L, m->gQ, sizeof(float) * rows * qd);
+  RV_ALLOC(L, m->gO, sizeof(float) * rows * qd);
+  RV_ALLOC(L, m->gLists, sizeof(int32_t) * rows * 2);
+  RV_ALLOC(L, m->gTokens, sizeof(int32_t) * rows);
+  m->ws_rows = rows;
+  return RV_OK;
+}
+
+// One decoder layer over all rows of the general path; rows are split by
+// route into two lists and each projection runs once per path.
+int enqueue_layer_rows(rv_model *m, int l, int B, int T, const int32_t *base, cudaStream_t s) {
+  const LayerDev &ly = m->layers[l];
+  const long M = (long)B * T;
+  const int32_t *lists[2] = {m->gLists, m->gLists + M};
+  const int32_t *cnt[2] = {m->d_counts, m->d_counts + 1};
+  const int act = m->act, d = m->d;
+  const int npath = m->has_river ? 2 : 1;
+  RV_CK(cudaMemcpyAsync(m->gHin, m->gH, sizeof(float) * M * d, cudaMemcpyDeviceToDevice, s));
+  RV_CK(launch_route_lists(m->st.route, B, T, m->gLists, (int)M, m->d_counts, s));
+  // attention sub-block
+  RV_CK(launch_rmsnorm_rows(m->gH, ly.attn_norm, d, m->c.rms_eps, act, m->gX, nullptr, m->d_nrows, (int)M, s));
+  for (int p = 0; p < npath; ++p)
+    RV_CK(launch_gemm_rows(make_mat(m, ly, MAT_QKV), p, act, m->gX, m->gY, lists[p], cnt[p], (int)M, s));
+  RopeRowsArgs ra{};
+  ra.kv = m->kv; ra.layer = l; ra.H = m->H; ra.Hkv = m->Hkv; ra.hd = m->hd; ra.act = act;
+  ra.Y = m->gY; ra.q = m->gQ; ra.rope_cs = m->rope_cs; ra.list = nullptr; ra.count = m->d_nrows;
+  ra.tokens_per_row = T; ra.base = base;
+  RV_CK(launch_rope_rows(ra, (int)M, s));
+  if (T == 1) {
+    AttnArgs at{};
+    at.kv = m->kv; at.layer = l; at.H = m->H; at.Hkv = m->Hkv; at.hd = m->hd; at.act = act;
+    at.q = m->gQ; at.o = m->gO; at.len = base; at.splits = m->attn_splits_max;
+    at.part = m->attn_part; at.counter = m->attn_counter;
+    // decode rows: split count sized for the batch
+    int sp = (2 * m->n_sm + m->Hkv * B - 1) / (m->Hkv * B);
+    if (sp < 1) sp = 1;
+    if (sp > m->attn_splits_max) sp = m->attn_splits_max;
+    at.splits = sp;
+    RV_CK(launch_attn_decode(at, B, s));
+  } else {
+    AttnRowsArgs ar{};
+    ar.kv = m->kv; ar.layer = l; ar.H = m->H; ar.Hkv = m->Hkv; ar.hd = m->hd; ar.act = act;
+    ar.q = m->gQ; ar.o = m->gO; ar.tokens_per_row = T; ar.base = base;
+    RV_CK(launch_attn_rows(ar, (int)M, s));
+  }
+  for (int p = 0; p < npath; ++p)
+    RV_CK(launch_gemm_rows(make_mat(m, ly, MAT_O), p, act, m->gO, m->gY2, lists[p], cnt[p], (int)M, s));
+  RV_CK(launch_resid_rows(m->gH, m->gY2, d, nullptr, m->d_nrows, (int)M, s));
+  // MLP sub-block
+  RV_CK(launch_rmsnorm_rows(m->gH, ly.mlp_norm, d, m->c.rms_eps, act, m->gX, nullptr, m->d_nrows, (int)M, s));
+  for (int p = 0; p < npath; ++p)
+    RV_CK(launch_gemm_rows(make_mat(m, ly, MAT_GU), p, act, m->gX, m->gY, lists[p], cnt[p], (int)M, s));
+  RV_CK(launch_swiglu_rows(m->gY, m->F, act, m->gX, nullptr, m->d_nrows, (int)M, s));
+  for (int p = 0; p < npath; ++p)
+    RV_CK(launch_gemm_rows(make_mat(m, ly, MAT_D), p, act, m->gX, m->gY2, lists[p], cnt[p], (int)M, s));
+  RV_CK(launch_resid_rows(m->gH, m->gY2, d, nullptr, m->d_nrows, (int)M, s));
+  return RV_OK;
+}
+
+// Final norm + LM head + argmax over rows Hf [B][d].
+int enqueue_head_rows(rv_model *m, int B, int bump_len, int set_len, cudaStream_t s) {
+  RV_CK(launch_rmsnorm_rows(m->gHf, m->final_norm, m->d, m->c.rms_eps, m->act, m->gXf, nullptr, m->d_nrows, B, s));
+  Mat lm{};
+  lm.w = m->lm_head; lm.N = m->V; lm.K = m->d;
+  RV_CK(launch_gemm_rows(lm, 0, m->act, m->gXf, m->gLogits, nullptr, m->d_nrows, B, s));
+  RV_CK(launch_argmax_rows(m->gLogits, m->V, B, m->st, bump_len, set_len, s));
+  if (m->debug)
+    RV_CK(cudaMemcpyAsync(m->dbg_logits, m->gLogits, sizeof(float) * B * m->V, cudaMemcpyDeviceToDevice, s));
+  return RV_OK;
+}
+
+int enqueue_step_rows(rv_model *m, int B, cudaStream_t s) {
+  const int L = m->L;
+  RV_CK(cudaMemsetAsync(m->st.err, 0, sizeof(int32_t), s));
+  RV_CK(launch_step_init(m->st, B, L, s));
+  RV_CK(launch_embed(m->embed, m->d, m->act, m->st.tokens, B, m->V, m->gH, m->debug ? m->dbg_h : nullptr, m->st.err,
+                     s));
+  for (int l = 0; l < L; ++l) {
+    int rc = enqueue_layer_rows(m, l, B, 1, m->st.len, s);
+    if (rc) return rc;
+    RV_CK(launch_decide_rows(m->st, m->gHin, m->gH, m->d, B, l + 1, L,
+                             m->debug ? m->dbg_s + (size_t)l * m->Bmax : nullptr, s));
+    if (m->debug)
+      RV_CK(cudaMemcpyAsync(m->dbg_h + (size_t)(l + 1) * m->Bmax * m->d, m->gH, sizeof(float) * B * m->d,
+                            cudaMemcpyDeviceToDevice, s));
+  }
+  RV_CK(cudaMemcpyAsync(m->gHf, m->gH, sizeof(float) * B * m->d, cudaMemcpyDeviceToDevice, s));
+  return enqueue_head_rows(m, B, 1, -1, s);
+}
+
+// Capture (once per batch size) and launch the decode-step graph.
+int launch_step(rv_model *m, int B) {
+  auto it = m->graphs.find(B);
+  if (it == m->graphs.end()) {
+    if (B > 1) {
+      int rc = ensure_ws(m, m->Bmax);
+      if (rc) return rc;
+    }
+    cudaGraph_t g = nullptr;
+    RV_CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
+    int rc = B == 1 ? enqueue_step_b1(m, m->stream) : enqueue_step_rows(m, B, m->stream);
+    cudaError_t ec = cudaStreamEndCapture(m->stream, &g);
+    if (rc != RV_OK) {
+      if (g) cudaGraphDestroy(g);
+      return rc;
+    }
+    if (ec != cudaSuccess) return fail(RV_ECUDA, "graph capture failed: %s", cudaGetErrorString(ec));
+    cudaGraphExec_t ge = nullptr;
+    cudaError_t ei = cudaGraphInstantiate(&ge, g, 0);
+    cudaGraphDestroy(g);
+    if (ei != cudaSuccess) return fail(RV_ECUDA, "graph instantiate failed: %s", cudaGetErrorString(ei));
+    it = m->graphs.emplace(B, ge).first;
+  }
+  RV_CK(cudaGraphLaunch(it->second, m->stream));
+  return RV_OK;
+}
+
+int check_common(rv_model *m) {
+  if (!m) return fail(RV_EINVAL, "null model");
+  return RV_OK;
+}
+
+int set_scalars(rv_model *m, int mode, float tau, int nrows) {
+  int32_t *in = pin_in(m);
+  const int B = m->Bmax;
+  in[2 * B] = mode;
+  memcpy(&in[2 * B + 1], &tau, sizeof(float));
+  in[2 * B + 2] = m->entry;
+  in[2 * B + 3] = nrows;
+  return RV_OK;
+}
+
+// Scalars of the state block written in stream order (device-pointer API).
+__global__ void k_set_scalars(int32_t *in, int Bmax, int mode, float tau, int entry, int nrows) {
+  in[2 * Bmax] = mode;
+  in[2 * Bmax + 1] = __float_as_int(tau);
+  in[2 * Bmax + 2] = entry;
+  in[2 * Bmax + 3] = nrows;
+}
+
+}  // namespace
+
+// ==================================================================== C ABI
+
+extern "C" {
+
+const char *rv_last_error(void) { return g_err.c_str(); }
+
+void rv_free_model(rv_model *m) {
+  if (!m) return;
+  if (m->stream) cudaStreamSynchronize(m->stream);
+  drop_graphs(m);
+  free_list(m->ws_allocs);
+  free_list(m->river_allocs);
+  free_list(m->allocs);
+  if (m->pinned) cudaFreeHost(m->pinned);
+  if (m->own_stream && m->stream) cudaStreamDestroy(m->stream);
+  delete m;
+}
+
+static int load_impl(rv_model *m, const rv_config *cfg, const void *const *weights) {
+  const rv_config &c = *cfg;
+  m->c = c;
+  m->act = c.act_dtype;
+  m->L = c.n_layers; m->d = c.d_model; m->H = c.n_heads; m->Hkv = c.n_kv_heads; m->hd = c.head_dim;
+  m->F = c.ffn; m->V = c.vocab; m->Bmax = c.max_batch; m->Tmax = c.max_seq;
+  m->qd = m->H * m->hd; m->kvd = m->Hkv * m->hd; m->qkv_n = m->qd + 2 * m->kvd;
+  RV_CK(cudaGetDevice(&m->dev));
+  RV_CK(cudaDeviceGetAttribute(&m->n_sm, cudaDevAttrMultiProcessorCount, m->dev));
+  const size_t e2 = 2;
+  const int d = m->d, F = m->F, V = m->V;
+  auto &A = m->allocs;
+  auto up = [&](uint16_t *dst, const void *src, size_t n) -> int {
+    RV_CK(cudaMemcpyAsync(dst, src, n * e2, cudaMemcpyHostToDevice, m->stream));
+    return RV_OK;
+  };
+#define RV_UP(dst, src, n)           \
+  do {                               \
+    int rc_ = up((dst), (src), (n)); \
+    if (rc_) return rc_;             \
+  } while (0)
+  RV_ALLOC(A, m->embed, e2 * V * d);
+  RV_UP(m->embed, weights[0], (size_t)V * d);
+  RV_ALLOC(A, m->final_norm, e2 * d);
+  RV_UP(m->final_norm, weights[1], d);
+  if (c.tied_embed) {
+    m->lm_head = m->embed;
+  } else {
+    RV_ALLOC(A, m->lm_head, e2 * V * d);
+    RV_UP(m->lm_head, weights[2], (size_t)V * d);
+  }
+  m->layers.resize(m->L);
+  for (int l = 0; l < m->L; ++l) {
+    const void *const *w = weights + 3 + 9 * l;
+    LayerDev &ly = m->layers[l];
+    RV_ALLOC(A, ly.attn_norm, e2 * d);
+    RV_UP(ly.attn_norm, w[0], d);
+    RV_ALLOC(A, ly.mlp_norm, e2 * d);
+    RV_UP(ly.mlp_norm, w[5], d);
+    RV_ALLOC(A, ly.w[MAT_QKV], e2 * m->qkv_n * d);
+    RV_UP(ly.w[MAT_QKV], w[1], (size_t)m->qd * d);
+    RV_UP(ly.w[MAT_QKV] + (size_t)m->qd * d, w[2], (size_t)m->kvd * d);
+    RV_UP(ly.w[MAT_QKV] + (size_t)(m->qd + m->kvd) * d, w[3], (size_t)m->kvd * d);
+    RV_ALLOC(A, ly.w[MAT_O], e2 * d * m->qd);
+    RV_UP(ly.w[MAT_O], w[4], (size_t)d * m->qd);
+    RV_ALLOC(A, ly.w[MAT_GU], e2 * 2 * F * d);
+    RV_UP(ly.w[MAT_GU], w[6], (size_t)F * d);
+    RV_UP(ly.w[MAT_GU] + (size_t)F * d, w[7], (size_t)F * d);
+    RV_ALLOC(A, ly.w[MAT_D], e2 * d * F);
+    RV_UP(ly.w[MAT_D], w[8], (size_t)d * F);
+  }
+  // the one KV cache, filled with the sentinel
+  m->kv.B = m->Bmax; m->kv.Hkv = m->Hkv; m->kv.T = m->Tmax; m->kv.hd = m->hd;
+  m->kv_bytes = (size_t)m->L * 2 * m->Bmax * m->Hkv * (size_t)m->Tmax * m->hd * e2;
+  RV_ALLOC(A, m->kv.base, m->kv_bytes);
+  RV_CK(launch_fill_u16(m->kv.base, m->kv_bytes / 2, KV_SENTINEL, m->stream));
+  RV_ALLOC(A, m->rope_cs, sizeof(float2) * (size_t)m->Tmax * (m->hd / 2));
+  RV_CK(launch_rope_table(m->rope_cs, m->Tmax, m->hd, (double)c.rope_theta, m->stream));
+  // step state
+  RV_ALLOC(A, m->d_state, sizeof(int32_t) * state_words(m->Bmax));
+  RV_CK(cudaMemsetAsync(m->d_state, 0, sizeof(int32_t) * state_words(m->Bmax), m->stream));
+  state_layout(m);
+  {
+    cudaError_t e = cudaMallocHost(&m->pinned, sizeof(int32_t) * (m->in_words + m->out_words + 2 * (size_t)m->Bmax));
+    if (e != cudaSuccess) {
+      m->pinned = nullptr;
+      return fail(RV_ENOMEM, "cudaMallocHost failed: %s", cudaGetErrorString(e));
+    }
+    memset(m->pinned, 0, sizeof(int32_t) * (m->in_words + m->out_words));
+  }
+  m->h_len.assign(m->Bmax, 0);
+  // batch-1 activations and reduction scratch
+  RV_ALLOC(A, m->hbuf[0], sizeof(float) * d);
+  RV_ALLOC(A, m->hbuf[1], sizeof(float) * d);
+  RV_ALLOC(A, m->hmid, sizeof(float) * d);
+  RV_ALLOC(A, m->qbuf, sizeof(float) * m->qd);
+  RV_ALLOC(A, m->obuf, sizeof(float) * m->qd);
+  RV_ALLOC(A, m->abuf, sizeof(float) * F);
+  RV_ALLOC(A, m->partials, sizeof(float) * 3 * 4 * (size_t)m->n_sm);
+  RV_ALLOC(A, m->counters, sizeof(unsigned) * (m->L + 4));
+  RV_CK(cudaMemsetAsync(m->counters, 0, sizeof(unsigned) * (m->L + 4), m->stream));
+  int sp = (2 * m->n_sm + m->Hkv - 1) / m->Hkv;
+  const int tiles = (m->Tmax + 31) / 32;
+  if (sp > tiles) sp = tiles;
+  if (sp > 128) sp = 128;
+  if (sp < 1) sp = 1;
+  m->attn_splits_b1 = sp;
+  m->attn_splits_max = sp;
+  RV_ALLOC(A, m->attn_part, sizeof(float) * (size_t)m->Bmax * m->H * sp * (m->hd + 2));
+  RV_ALLOC(A, m->attn_counter, sizeof(unsigned) * (size_t)m->Bmax * m->Hkv);
+  RV_CK(cudaMemsetAsync(m->attn_counter, 0, sizeof(unsigned) * (size_t)m->Bmax * m->Hkv, m->stream));
+  // head rows for the general path, identity list
+  RV_ALLOC(A, m->gHf, sizeof(float) * (size_t)m->Bmax * d);
+  RV_ALLOC(A, m->gXf, sizeof(float) * (size_t)m->Bmax * d);
+  RV_ALLOC(A, m->gLogits, sizeof(float) * (size_t)m->Bmax * V);
+  RV_CK(cudaStreamSynchronize(m->stream));
+  return RV_OK;
+}
+
+int rv_load_model(const rv_config *cfg, const void *const *weights, void *stream, rv_model **out) {
+  g_err.clear();
+  if (!cfg || !weights || !out) return fail(RV_EINVAL, "null argument");
+  *out = nullptr;
+  const rv_config &c = *cfg;
+  if (c.n_layers < 1 || c.d_model < 8 || c.n_heads < 1 || c.n_kv_heads < 1 || c.n_heads % c.n_kv_heads ||
+      (c.head_dim != 64 && c.head_dim != 128) || c.ffn < 8 || c.vocab < 2 || c.max_batch < 1 || c.max_seq < 1 ||
+      (c.act_dtype != 0 && c.act_dtype != 1) || c.d_model % 32 || c.ffn % 16 ||
+      (c.n_heads / c.n_kv_heads) > 8 || !(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f))
+    return fail(RV_EINVAL, "unsupported configuration (d_model %% 32, ffn %% 16, head_dim 64/128, H/Hkv <= 8)");
+  if ((long)c.max_batch * c.max_seq > (1L << 31) || c.max_batch > 4096)
+    return fail(RV_EINVAL, "max_batch x max_seq too large");
+  const int nw = 3 + 9 * c.n_layers;
+  for (int i = 0; i < nw; ++i)
+    if (!weights[i] && !(i == 2 && c.tied_embed)) return fail(RV_EINVAL, "weight %d is NULL", i);
+  rv_model *m = new (std::nothrow) rv_model();
+  if (!m) return fail(RV_ENOMEM, "host allocation failed");
+  if (stream) {
+    m->stream = static_cast<cudaStream_t>(stream);
+  } else {
+    cudaError_t e = cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) {
+      delete m;
+      return fail(RV_ECUDA, "cudaStreamCreate failed: %s", cudaGetErrorString(e));
+    }
+    m->own_stream = true;
+  }
+  int rc = load_impl(m, cfg, weights);
+  if (rc != RV_OK) {
+    std::string msg = g_err;
+    rv_free_model(m);
+    g_err = msg;
+    return rc;
+  }
+  *out = m;
+  return RV_OK;
+}
+
+int rv_quantize_river(rv_model *m, int group_size, int entry_layer) {
+  g_err.clear();
+  if (check_common(m)) return RV_EINVAL;
+  if (group_size < 32 || group_size % 32) return fail(RV_EINVAL, "group_size must be a positive multiple of 32");
+  if (entry_layer < 1 || entry_layer > m->L) return fail(RV_EINVAL, "entry_layer must be in 1..L");
+  RV_CK(cudaStreamSynchronize(m->stream));
+  drop_graphs(m);
+  free_list(m->river_allocs);
+  m->has_river = false;
+  m->group = group_size;
+  for (LayerDev &ly : m->layers)
+    for (int i = 0; i < N_MAT; ++i) ly.r[i] = RiverDev{};
+  RV_CK(cudaMemsetAsync(m->st.err, 0, sizeof(int32_t), m->stream));
+  for (LayerDev &ly : m->layers) {
+    for (int i = 0; i < N_MAT; ++i) {
+      Mat mt = make_mat(m, ly, i);
+      RiverDev &r = ly.r[i];
+      r.Kp = round32(mt.K);
+      r.G = (mt.K + group_size - 1) / group_size;
+      auto &A = m->river_allocs;
+      RV_ALLOC(A, r.q, sizeof(uint32_t) * (size_t)mt.N * (r.Kp / 8));
+      RV_ALLOC(A, r.s, sizeof(__half) * (size_t)mt.N * r.G);
+      RV_ALLOC(A, r.z, sizeof(__half) * (size_t)mt.N * r.G);
+      RV_CK(launch_rtn_quantize(mt.w, mt.N, mt.K, m->act, group_size, r.Kp, r.q, r.s, r.z, m->st.err, m->stream));
+    }
+  }
+  int32_t err = 0;
+  RV_CK(cudaMemcpyAsync(&err, m->st.err, sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
+  RV_CK(cudaStreamSynchronize(m->stream));
+  if (err & 4) {
+    free_list(m->river_allocs);
+    return fail(RV_EINVAL, "a group's scale overflows fp16");
+  }
+  m->has_river = true;
+  m->entry = entry_layer;
+  return RV_OK;
+}
+
+int rv_export_river(const rv_model *m, int layer, int proj, void *q_packed, void *scales, void *zeros) {
+  g_err.clear();
+  if (!m) return fail(RV_EINVAL, "null model");
+  if (!m->has_river) return fail(RV_ESTATE, "river not built");
+  if (layer < 1 || layer > m->L || proj < 0 || proj > 6) return fail(RV_EINVAL, "bad layer or projection");
+  int mat, row0, rows, K;
+  switch (proj) {
+    case RV_PROJ_Q: mat = MAT_QKV; row0 = 0; rows = m->qd; K = m->d; break;
+    case RV_PROJ_K: mat = MAT_QKV; row0 = m->qd; rows = m->kvd; K = m->d; break;
+    case RV_PROJ_V: mat = MAT_QKV; row0 = m->qd + m->kvd; rows = m->kvd; K = m->d; break;
+    case RV_PROJ_O: mat = MAT_O; row0 = 0; rows = m->d; K = m->qd; break;
+    case RV_PROJ_GATE: mat = MAT_GU; row0 = 0; rows = m->F; K = m->d; break;
+    case RV_PROJ_UP: mat = MAT_GU; row0 = m->F; rows = m->F; K = m->d; break;
+    default: mat = MAT_D; row0 = 0; rows = m->d; K = m->F; break;
+  }
+  const RiverDev &r = m->layers[layer - 1].r[mat];
+  if (q_packed)
+    RV_CK(cudaMemcpy2D(q_packed, sizeof(uint32_t) * (K / 8), r.q + (size_t)row0 * (r.Kp / 8), sizeof(uint32_t) * (r.Kp / 8),
+                       sizeof(uint32_t) * (K / 8), rows, cudaMemcpyDeviceToHost));
+  if (scales) RV_CK(cudaMemcpy(scales, r.s + (size_t)row0 * r.G, sizeof(__half) * (size_t)rows * r.G, cudaMemcpyDeviceToHost));
+  if (zeros) RV_CK(cudaMemcpy(zeros, r.z + (size_t)row0 * r.G, sizeof(__half) * (size_t)rows * r.G, cudaMemcpyDeviceToHost));
+  return RV_OK;
+}
+
+static int validate_step(rv_model *m, int B, const int32_t *forced_host, bool forced_given) {
+  if (B < 1 || B > m->Bmax) return fail(RV_EINVAL, "B must be in 1..max_batch");
+  if (!forced_given && !m->has_river) return fail(RV_ESTATE, "tau-rule decode needs rv_quantize_river first");
+  if (forced_host)
+    for (int b = 0; b < B; ++b) {
+      if (forced_host[b] < 0 || forced_host[b] > m->L) return fail(RV_EINVAL, "forced exit out of range");
+      if (forced_host[b] < m->L && !m->has_river) return fail(RV_ESTATE, "forced exit below L needs the river");
+    }
+  for (int b = 0; b < B; ++b)
+    if (m->h_len[b] >= m->Tmax) return fail(RV_ECAPACITY, "row %d: KV cache full (%d positions)", b, m->Tmax);
+  return RV_OK;
+}
+
+int rv_decode_step(rv_model *m, const int32_t *tokens, int B, float tau, const int32_t *forced_exit,
+                   int32_t *next_ids, int32_t *exit_layer) {
+  g_err.clear();
+  if (check_common(m)) return RV_EINVAL;
+  if (!tokens || !next_ids || !exit_layer) return fail(RV_EINVAL, "null pointer");
+  int rc = validate_step(m, B, forced_exit, forced_exit != nullptr);
+  if (rc) return rc;
+  for (int b = 0; b < B; ++b)
+    if (tokens[b] < 0 || tokens[b] >= m->V) return fail(RV_EINVAL, "token %d out of range", tokens[b]);
+  if (!(tau == tau)) return fail(RV_EINVAL, "tau is NaN");
+  int32_t *in = pin_in(m);
+  memcpy(in, tokens, sizeof(int32_t) * B);
+  if (forced_exit) memcpy(in + m->Bmax, forced_exit, sizeof(int32_t) * B);
+  set_scalars(m, forced_exit ? 1 : 0, tau, B);
+  RV_CK(cudaMemcpyAsync(m->d_state, in, sizeof(int32_t) * m->in_words, cudaMemcpyHostToDevice, m->stream));
+  rc = launch_step(m, B);
+  if (rc) return rc;
+  int32_t *out = pin_out(m);
+  RV_CK(cudaMemcpyAsync(out, m->st.next_ids, sizeof(int32_t) * m->out_words, cudaMemcpyDeviceToHost, m->stream));
+  RV_CK(cudaStreamSynchronize(m->stream));
+  if (out[2 * m->Bmax]) return fail(RV_EINVAL, "device flagged an invalid input (0x%x)", out[2 * m->Bmax]);
+  memcpy(next_ids, out, sizeof(int32_t) * B);
+  memcpy(exit_layer, out + m->Bmax, sizeof(int32_t) * B);
+  for (int b = 0; b < B; ++b) m->h_len[b] += 1;
+  return RV_OK;
+}
+
+int rv_decode_step_dev(rv_model *m, const int32_t *d_tokens, int B, float tau, const int32_t *d_forced_exit,
+                       int32_t *d_next_ids, int32_t *d_exit_layer) {
+  g_err.clear();
+  if (check_common(m)) return RV_EINVAL;
+  if (!d_tokens || !d_next_ids || !d_exit_layer) return fail(RV_EINVAL, "null pointer");
+  int rc = validate_step(m, B, nullptr, d_forced_exit != nullptr);
+  if (rc) return rc;
+  if (d_forced_exit && !m->has_river) return fail(RV_ESTATE, "forced exits need the river");
+  if (!(tau == tau)) return fail(RV_EINVAL, "tau is NaN");
+  RV_CK(cudaMemcpyAsync(m->d_state, d_tokens, sizeof(int32_t) * B, cudaMemcpyDeviceToDevice, m->stream));
+  if (d_forced_exit)
+    RV_CK(cudaMemcpyAsync(m->d_state + m->Bmax, d_forced_exit, sizeof(int32_t) * B, cudaMemcpyDeviceToDevice,
+                          m->stream));
+  k_set_scalars<<<1, 1, 0, m->stream>>>(m->d_state, m->Bmax, d_forced_exit ? 1 : 0, tau, m->entry, B);
+  RV_CK(cudaGetLastError());
+  rc = launch_step(m, B);
+  if (rc) return rc;
+  RV_CK(cudaMemcpyAsync(d_next_ids, m->st.next_ids, sizeof(int32_t) * B, cudaMemcpyDeviceToDevice, m->stream));
+  RV_CK(cudaMemcpyAsync(d_exit_layer, m->st.exit_layer, sizeof(int32_t) * B, cudaMemcpyDeviceToDevice, m->stream));
+  for (int b = 0; b < B; ++b) m->h_len[b] += 1;
+  return RV_OK;
+}
+
+int rv_sync_status(rv_model *m) {
+  g_err.clear();
+  if (check_common(m)) return RV_EINVAL;
+  int32_t err = 0;
+  RV_CK(cudaMemcpyAsync(&err, m->st.err, sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
+  RV_CK(cudaStreamSynchronize(m->stream));
+  if (err) return fail(RV_EINVAL, "device flagged an invalid input (0x%x)", err);
+  return RV_OK;
+}
+
+int rv_prefill(rv_model *m, const int32_t *tokens, int B, int T0, float tau, int fixed_exit_layer,
+               int32_t *next_ids, int32_t *exit_layer) {
+  g_err.clear();
+  if (check_common(m)) return RV_EINVAL;
+  if (!tokens || !next_ids || !exit_layer) return fail(RV_EINVAL, "null pointer");
+  if (B < 1 || B > m->Bmax || T0 < 1 || T0 > m->Tmax) return fail(RV_EINVAL, "B or T0 out of range");
+  if (fixed_exit_layer < -1 || fixed_exit_layer > m->L) return fail(RV_EINVAL, "fixed_exit_layer out of range");
+  if (!m->has_river && fixed_exit_layer != m->L) return fail(RV_ESTATE, "prefill with exits needs the river");
+  if (!(tau == tau)) return fail(RV_EINVAL, "tau is NaN");
+  const long M = (long)B * T0;
+  if (M > (1L << 24)) return fail(RV_EINVAL, "B x T0 too large");
+  for (long i = 0; i < M; ++i)
+    if (tokens[i] < 0 || tokens[i] >= m->V) return fail(RV_EINVAL, "token %d out of range", tokens[i]);
+  RV_CK(cudaStreamSynchronize(m->stream));
+  int rc = ensure_ws(m, M > m->Bmax ? M : m->Bmax);
+  if (rc) return rc;
+  cudaStream_t s = m->stream;
+  RV_CK(cudaMemcpy(m->gTokens, tokens, sizeof(int32_t) * M, cudaMemcpyHostToDevice));
+  int32_t *in = pin_in(m);
+  for (int b = 0; b < B; ++b) in[m->Bmax + b] = fixed_exit_layer;
+  set_scalars(m, fixed_exit_layer >= 0 ? 1 : 0, tau, (int)M);
+  RV_CK(cudaMemcpyAsync(m->d_state, in, sizeof(int32_t) * m->in_words, cudaMemcpyHostToDevice, s));
+  RV_CK(cudaMemsetAsync(m->st.err, 0, sizeof(int32_t), s));
+  RV_CK(launch_step_init(m->st, B, m->L, s));
+  RV_CK(launch_embed(m->embed, m->d, m->act, m->gTokens, (int)M, m->V, m->gH, nullptr, m->st.err, s));
+  if (m->debug) RV_CK(launch_copy_rows(m->gH + (size_t)(T0 - 1) * m->d, T0 * m->d, m->dbg_h, m->d, m->d, B, s));
+  for (int l = 0; l < m->L; ++l) {
+    rc = enqueue_layer_rows(m, l, B, T0, nullptr, s);
+    if (rc) return rc;
+    RV_CK(launch_seq_decide(m->st, m->gHin, m->gH, m->d, B, T0, l + 1, m->L, fixed_exit_layer,
+                            m->debug ? m->dbg_s + (size_t)l * m->Bmax : nullptr, s));
+    if (m->debug)
+      RV_CK(launch_copy_rows(m->gH + (size_t)(T0 - 1) * m->d, T0 * m->d, m->dbg_h + (size_t)(l + 1) * m->Bmax * m->d,
+                             m->d, m->d, B, s));
+  }
+  RV_CK(launch_copy_rows(m->gH + (size_t)(T0 - 1) * m->d, T0 * m->d, m->gHf, m->d, m->d, B, s));
+  // the head runs over B rows: nrows = B (written in-stream; the pinned block may still be in flight)
+  k_set_scalars<<<1, 1, 0, s>>>(m->d_state, m->Bmax, fixed_exit_layer >= 0 ? 1 : 0, tau, m->entry, B);
+  RV_CK(cudaGetLastError());
+  rc = enqueue_head_rows(m, B, 0, T0, s);
+  if (rc) return rc;
+  int32_t *out = pin_out(m);
+  RV_CK(cudaMemcpyAsync(out, m->st.next_ids, sizeof(int32_t) * m->out_words, cudaMemcpyDeviceToHost, s));
+  RV_CK(cudaStreamSynchronize(s));
+  if (out[2 * m->Bmax]) return fail(RV_EINVAL, "device flagged an invalid input (0x%x)", out[2 * m->Bmax]);
+  memcpy(next_ids, out, sizeof(int32_t) * B);
+  memcpy(exit_layer, out + m->Bmax, sizeof(int32_t) * B);
+  for (int b = 0; b < B; ++b) m->h_len[b] = T0;
+  return RV_OK;
+}
+
+int rv_kv_reset(rv_model *m, const int32_t *rows, int n_rows) {
+  g_err.clear();
+  if (check_common(m)) return RV_EINVAL;
+  const int n = rows ? n_rows : m->Bmax;
+  if (rows && n_rows < 0) return fail(RV_EINVAL, "n_rows < 0");
+  for (int i = 0; i < n; ++i) {
+    const int b = rows ? rows[i] : i;
+    if (b < 0 || b >= m->Bmax) return fail(RV_EINVAL, "row %d out of range", b);
+  }
+  RV_CK(cudaStreamSynchronize(m->stream));
+  if (!rows) {
+    RV_CK(launch_fill_u16(m->kv.base, m->kv_bytes / 2, KV_SENTINEL, m->stream));
+  } else {
+    const size_t per = (size_t)m->Hkv * m->Tmax * m->hd;
+    for (int i = 0; i < n; ++i)
+      for (int l = 0; l < m->L; ++l)
+        for (int kvi = 0; kvi < 2; ++kvi)
+          RV_CK(launch_fill_u16(m->kv.base + m->kv.idx(l, kvi, rows[i], 0, 0), per, KV_SENTINEL, m->stream));
+  }
+  for (int i = 0; i < n; ++i) {
+    const int b = rows ? rows[i] : i;
+    m->h_len[b] = 0;
+  }
+  RV_CK(cudaMemcpyAsync(m->st.len, m->h_len.data(), sizeof(int32_t) * m->Bmax, cudaMemcpyHostToDevice, m->stream));
+  RV_CK(cudaStreamSynchronize(m->stream));
+  return RV_OK;
+}
+
+int rv_set_debug(rv_model *m, int enable) {
+  g_err.clear();
+  if (check_common(m)) return RV_EINVAL;
+  RV_CK(cudaStreamSynchronize(m->stream));
+  if (enable && !m->dbg_h) {
+    auto &A = m->allocs;
+    RV_ALLOC(A, m->dbg_h, sizeof(float) * (size_t)(m->L + 1) * m->Bmax * m->d);
+    RV_ALLOC(A, m->dbg_s, sizeof(float) * (size_t)m->L * m->Bmax);
+    RV_ALLOC(A, m->dbg_logits, sizeof(float) * (size_t)m->Bmax * m->V);
+    RV_CK(cudaMemset(m->dbg_h, 0, sizeof(float) * (size_t)(m->L + 1) * m->Bmax * m->d));
+    RV_CK(cudaMemset(m->dbg_s, 0xff, sizeof(float) * (size_t)m->L * m->Bmax));
+    RV_CK(cudaMemset(m->dbg_logits, 0, sizeof(float) * (size_t)m->Bmax * m->V));
+  }
+  if ((bool)enable != m->debug) drop_graphs(m);
+  m->debug = enable != 0;
+  return RV_OK;
+}
+
+int rv_debug_dump(rv_model *m, int what, void *dst, size_t bytes) {
+  g_err.clear();
+  if (check_common(m)) return RV_EINVAL;
+  if (!dst) return fail(RV_EINVAL, "null dst");
+  RV_CK(cudaStreamSynchronize(m->stream));
+  const void *src = nullptr;
+  size_t need = 0;
+  switch (what) {
+    case RV_DUMP_HIDDEN: src = m->dbg_h; need = sizeof(float) * (size_t)(m->L + 1) * m->Bmax * m->d; break;
+    case RV_DUMP_S: src = m->dbg_s; need = sizeof(float) * (size_t)m->L * m->Bmax; break;
+    case RV_DUMP_LOGITS: src = m->dbg_logits; need = sizeof(float) * (size_t)m->Bmax * m->V; break;
+    case RV_DUMP_KV: src = m->kv.base; need = m->kv_bytes; break;
+    case RV_DUMP_LENS:
+      if (bytes != sizeof(int32_t) * m->Bmax) return fail(RV_EINVAL, "size mismatch");
+      RV_CK(cudaMemcpy(dst, m->st.len, bytes, cudaMemcpyDeviceToHost));
+      return RV_OK;
+    default: return fail(RV_EINVAL, "unknown dump id");
+  }
+  if (!src) return fail(RV_ESTATE, "debug buffers not enabled (rv_set_debug)");
+  if (bytes != need) return fail(RV_EINVAL, "size mismatch: need %zu bytes", need);
+  RV_CK(cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost));
+  return RV_OK;
+}
+
+size_t rv_kv_bytes(const rv_model *m) { return m ? m->kv_bytes : 0; }
+
+size_t rv_param_bytes(const rv_model *m, int which) {
+  if (!m) return 0;
+  size_t t = 0;
+  if (which == 0) {
+    const size_t d = m->d;
+    t = 2 * ((size_t)m->V * d * (m->c.tied_embed ? 1 : 2) + d);
+    t += (size_t)m->L * 2 * (2 * d + (size_t)m->qkv_n * d + d * m->qd + 2 * (size_t)m->F * d + d * m->F);
+    return t;
+  }
+  if (!m->has_river) return 0;
+  for (const LayerDev &ly : m->layers)
+    for (int i = 0; i < N_MAT; ++i) {
+      const int N = i == MAT_QKV ? m->qkv_n : i == MAT_GU ? 2 * m->F : m->d;
+      t += (size_t)N * (ly.r[i].Kp / 2) + 2 * sizeof(__half) * (size_t)N * ly.r[i].G;
+    }
+  return t;
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// Device helpers and data layouts shared by the River-LLM CUDA kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define RV_WARP 32
+
+namespace rv {
+
+// ------------------------------------------------------------------ 16-bit
+// act = 0: fp16, act = 1: bf16.  Values that enter a matrix product are kept
+// as fp32 numbers that are exactly representable in the 16-bit type.
+
+__device__ __forceinline__ float act_to_f(uint16_t b, int act) {
+  if (act) return __uint_as_float(((uint32_t)b) << 16);
+  return __half2float(__ushort_as_half(b));
+}
+
+__device__ __forceinline__ uint16_t f_to_act(float x, int act) {
+  if (act) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  return __half_as_ushort(__float2half_rn(x));
+}
+
+__device__ __forceinline__ float round_act(float x, int act) { return act_to_f(f_to_act(x, act), act); }
+
+// ------------------------------------------------------------------ reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Sum over the block; every thread gets the result.  scratch >= 32 floats.
+__device__ __forceinline__ float block_sum(float v, float *scratch) {
+  int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) scratch[wid] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int i = 0; i < nw; ++i) t += scratch[i];  // fixed order: deterministic
+  return t;
+}
+
+// ------------------------------------------------------------------ weights
+
+// River copy of one projection in the device layout: canonical packing with
+// the row stride padded to Kp (a multiple of 32) nibbles; fp16 scale and zero
+// per (row, group of g columns).
+struct RiverMat {
+  const uint32_t *q;  // [N][Kp/8]
+  const __half *s;    // [N][G]
+  const __half *z;    // [N][G]
+  int Kp, G, g;
+};
+
+// One projection: backbone 16-bit matrix [N][K] and its river copy.
+struct Mat {
+  const uint16_t *w;
+  RiverMat r;
+  int N, K;
+};
+
+// Per-step device state (all pointers into one device block).
+struct StepState {
+  const int32_t *tokens;  // [B]
+  const int32_t *forced;  // [B] forced exit layers (mode 1)
+  int32_t *route;         // [B] 0 backbone, 1 river
+  int32_t *exit_layer;    // [B]
+  int32_t *len;           // [B] cached positions (position of the token being decoded)
+  int32_t *next_ids;      // [B]
+  const float *tau;       // scalar
+  const int32_t *mode;    // scalar: 0 tau rule, 1 forced exits
+  const int32_t *entry;   // scalar: first layer eligible for the tau rule
+  int32_t *err;           // scalar error flags (bit 0 token, bit 1 forced value, bit 2 quant)
+};
+
+// KV cache geometry: [L][2][max_batch][Hkv][max_seq][hd] 16-bit.
+struct KVGeom {
+  uint16_t *base;
+  int B, Hkv, T, hd;
+  __host__ __device__ size_t idx(int l, int kv, int b, int g, int p) const {
+    return ((((size_t)l * 2 + kv) * B + b) * Hkv + g) * (size_t)T * hd + (size_t)p * hd;
+  }
+};
+
+}  // namespace rv

@@ -1,0 +1,128 @@
+// Kernel argument blocks and host launchers of librv (internal header).
+#pragma once
+
+#include "common.cuh"
+
+namespace rv {
+
+enum { PRO_NORM = 0, PRO_VEC = 1 };
+enum { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_DOWN = 3, EPI_LOGITS = 4 };
+
+// Arguments of the batch-1 GEMV kernels (see decode_b1.cu).
+struct GemvArgs {
+  Mat m;
+  int units;  // output rows (or row pairs) to produce
+  // prologue
+  const float *h;         // PRO_NORM: residual stream [K]
+  const uint16_t *gamma;  // PRO_NORM: RMSNorm gain [K]
+  float eps;
+  const float *vec;       // PRO_VEC: activation [K]
+  // epilogue
+  const float *h_base;  // EPI_RESID / EPI_DOWN: residual added to
+  float *h_out;         // EPI_RESID / EPI_DOWN
+  const float *h_in;    // EPI_DOWN: layer input, for s(l)
+  float *out_vec;       // EPI_QKV: q [H*hd]; EPI_SWIGLU: a [F]
+  KVGeom kv;
+  int layer;            // 0-based
+  int L, H, Hkv, hd;
+  const float2 *rope_cs;  // [max_seq][hd/2] (cos, sin)
+  float *partials;
+  unsigned *counter;
+  float *dbg_h;       // EPI_DOWN: hidden dump for this layer (row 0) or NULL
+  float *dbg_s;       // EPI_DOWN: s dump for this layer or NULL
+  float *dbg_logits;  // EPI_LOGITS: logits dump or NULL
+  StepState st;
+};
+
+// Exit decision for row b after layer layer1 (1-based) from the three sums
+// sum(h_in*h_out), sum(h_in^2), sum(h_out^2).  One thread calls it.
+// s = dot / max(|h_in| |h_out|, 1e-8); strict s > tau (aitrends.kr).
+__device__ __forceinline__ void decide_row(const StepState &st, int b, int layer1, int L, float dot, float n1,
+                                           float n2, float *dbg_s) {
+  if (st.route[b] != 0) {
+    if (dbg_s) dbg_s[b] = __int_as_float(0x7fc00000);
+    return;
+  }
+  const float den = fmaxf(sqrtf(n1) * sqrtf(n2), 1e-8f);
+  const float s = dot / den;
+  if (dbg_s) dbg_s[b] = s;
+  if (*st.mode == 1) {
+    int f = st.forced[b];
+    if (f < 0 || f > L) f = L;
+    if (layer1 == f && layer1 < L) { st.route[b] = 1; st.exit_layer[b] = layer1; }
+  } else if (layer1 >= *st.entry && layer1 <= L - 1 && s > *st.tau) {
+    st.route[b] = 1;
+    st.exit_layer[b] = layer1;
+  }
+}
+
+cudaError_t launch_gemv_b1(int act, int pro, int epi, const GemvArgs &a, int grid, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention
+struct AttnArgs {
+  KVGeom kv;
+  int layer, H, Hkv, hd, act;
+  const float *q;      // [B][H*hd] (act16-rounded, after RoPE)
+  float *o;            // [B][H*hd] output (act16-rounded)
+  const int32_t *len;  // [B]: the token being decoded sits at position len[b]
+  int splits;
+  float *part;         // [B][H][splits][hd + 2]
+  unsigned *counter;   // [B][Hkv]
+};
+cudaError_t launch_attn_decode(const AttnArgs &a, int B, cudaStream_t s);
+
+// Causal attention for token rows of the general path: row m of the list
+// attends to positions 0..pos(m) of its sequence.
+struct AttnRowsArgs {
+  KVGeom kv;
+  int layer, H, Hkv, hd, act;
+  const float *q;  // [M][H*hd]
+  float *o;        // [M][H*hd]
+  const int32_t *list;
+  const int32_t *count;
+  int tokens_per_row;    // T: token m belongs to sequence m / T, position base + m % T
+  const int32_t *base;   // [B] position of the row's first token (decode: len; prefill: NULL = 0)
+};
+cudaError_t launch_attn_rows(const AttnRowsArgs &a, int max_rows, cudaStream_t s);
+
+// ---------------------------------------------------------------- general path
+cudaError_t launch_embed(const uint16_t *E, int d, int act, const int32_t *tokens, int M, int vocab, float *H,
+                         float *dbg_h, int32_t *err, cudaStream_t s);
+cudaError_t launch_step_init(const StepState &st, int B, int L, cudaStream_t s);
+cudaError_t launch_route_lists(const int32_t *route, int B, int T, int32_t *lists, int list_stride,
+                               int32_t *counts, cudaStream_t s);
+cudaError_t launch_rmsnorm_rows(const float *H, const uint16_t *gamma, int d, float eps, int act, float *X,
+                                const int32_t *list, const int32_t *count, int max_rows, cudaStream_t s);
+cudaError_t launch_gemm_rows(const Mat &m, int river, int act, const float *X, float *Y, const int32_t *list,
+                             const int32_t *count, int max_rows, cudaStream_t s);
+struct RopeRowsArgs {
+  KVGeom kv;
+  int layer, H, Hkv, hd, act;
+  const float *Y;  // [M][(H+2Hkv)*hd]
+  float *q;        // [M][H*hd]
+  const float2 *rope_cs;
+  const int32_t *list, *count;
+  int tokens_per_row;
+  const int32_t *base;
+};
+cudaError_t launch_rope_rows(const RopeRowsArgs &a, int max_rows, cudaStream_t s);
+cudaError_t launch_resid_rows(float *H, const float *Y, int d, const int32_t *list, const int32_t *count,
+                              int max_rows, cudaStream_t s);
+cudaError_t launch_swiglu_rows(const float *Y, int F, int act, float *A, const int32_t *list,
+                               const int32_t *count, int max_rows, cudaStream_t s);
+cudaError_t launch_decide_rows(const StepState &st, const float *Hin, const float *H, int d, int B, int layer1,
+                               int L, float *dbg_s, cudaStream_t s);
+cudaError_t launch_seq_decide(const StepState &st, const float *Hin, const float *H, int d, int B, int T,
+                              int layer1, int L, int fixed_exit, float *dbg_smin, cudaStream_t s);
+cudaError_t launch_argmax_rows(const float *logits, int V, int B, StepState st, int bump_len, int set_len,
+                               cudaStream_t s);
+cudaError_t launch_copy_rows(const float *src, int src_stride, float *dst, int dst_stride, int d, int B,
+                             cudaStream_t s);
+
+// ---------------------------------------------------------------- river construction
+cudaError_t launch_rtn_quantize(const uint16_t *W, int N, int K, int act, int g, int Kp, uint32_t *q, __half *sc,
+                                __half *zp, int32_t *err, cudaStream_t s);
+cudaError_t launch_rope_table(float2 *cs, int T, int hd, double theta, cudaStream_t s);
+cudaError_t launch_fill_u16(uint16_t *p, size_t n, uint16_t v, cudaStream_t s);
+
+}  // namespace rv
