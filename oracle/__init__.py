@@ -58,6 +58,8 @@ def lib():
         "ora_prefill": ([vp, vp, i32, i32, dbl, i32, vp, vp, vp, vp, vp, vp, vp, vp], i32),
         "ora_decode_step": ([vp, vp, i32, dbl, vp, vp, vp, vp, vp, vp, vp, vp, vp], i32),
         "ora_kv_reset": ([vp, vp, i32], i32),
+        "ora_layer_forward": ([vp, i32, i32, vp, vp, vp], i32),
+        "ora_head": ([vp, i32, vp, vp, vp], i32),
         "ora_get_kv": ([vp, vp, ctypes.c_size_t], i32),
         "ora_set_kv": ([vp, vp, ctypes.c_size_t, vp], i32),
         "ora_get_lens": ([vp, vp], i32),
@@ -250,6 +252,27 @@ class Model:
         if debug:
             out.update(hidden=hid, s=ss, logits=lg)
         return out
+
+    def layer_forward(self, layer: int, h_in, river) -> np.ndarray:
+        """Layer `layer` (1-based) for rows 0..B-1 at their current positions."""
+        h = np.ascontiguousarray(h_in, dtype=np.float64)
+        B = h.shape[0]
+        rv = np.ascontiguousarray(river, dtype=np.int32).reshape(-1)
+        out = np.zeros_like(h)
+        rc = lib().ora_layer_forward(self._h, layer, B, _p(rv), _p(h), _p(out))
+        if rc != RV_OK:
+            raise RuntimeError(f"ora_layer_forward failed: {rc}")
+        return out
+
+    def head(self, h):
+        h = np.ascontiguousarray(h, dtype=np.float64)
+        B = h.shape[0]
+        logits = np.zeros((B, self.shape.vocab))
+        ids = np.zeros(B, dtype=np.int32)
+        rc = lib().ora_head(self._h, B, _p(h), _p(logits), _p(ids))
+        if rc != RV_OK:
+            raise RuntimeError(f"ora_head failed: {rc}")
+        return logits, ids
 
     def kv_bytes(self) -> int:
         return int(lib().ora_kv_bytes(self._h))

@@ -687,6 +687,45 @@ int ora_decode_step(ora_model *m, const int32_t *tokens, int B, double tau, cons
 }
 
 /* ------------------------------------------------------------------ */
+/* Single layer / head entry points (for layer-by-layer checks)        */
+/* ------------------------------------------------------------------ */
+
+int ora_layer_forward(ora_model *m, int layer, int B, const int32_t *river, const double *h_in, double *h_out) {
+  if (!m || !river || !h_in || !h_out || layer < 1 || layer > m->c.n_layers || B < 1 || B > m->c.max_batch)
+    return RV_EINVAL;
+  const int d = m->c.d_model;
+  for (int b = 0; b < B; ++b) {
+    if (river[b] && !m->has_river) return RV_ESTATE;
+    if (m->len[b] >= m->c.max_seq) return RV_ECAPACITY;
+  }
+  double *Hsub = (double *)malloc(sizeof(double) * (size_t)B * d);
+  int *row = (int *)malloc(sizeof(int) * (size_t)B), *pos = (int *)malloc(sizeof(int) * (size_t)B);
+  for (int path = 0; path < 2; ++path) {
+    int n = 0;
+    for (int b = 0; b < B; ++b)
+      if ((river[b] != 0) == path) {
+        row[n] = b; pos[n] = m->len[b];
+        memcpy(Hsub + (size_t)n * d, h_in + (size_t)b * d, sizeof(double) * d);
+        n++;
+      }
+    if (!n) continue;
+    layer_apply(m, layer - 1, path, n, row, pos, Hsub);
+    for (int i = 0; i < n; ++i) memcpy(h_out + (size_t)row[i] * d, Hsub + (size_t)i * d, sizeof(double) * d);
+  }
+  free(Hsub); free(row); free(pos);
+  return RV_OK;
+}
+
+int ora_head(ora_model *m, int B, const double *h, double *logits, int32_t *ids) {
+  if (!m || !h || !logits || !ids || B < 1) return RV_EINVAL;
+  for (int b = 0; b < B; ++b) {
+    int f = 0;
+    ids[b] = lm_head_pick(m, h + (size_t)b * m->c.d_model, logits + (size_t)b * m->c.vocab, -1, &f);
+  }
+  return RV_OK;
+}
+
+/* ------------------------------------------------------------------ */
 /* Model lifetime and cache access                                     */
 /* ------------------------------------------------------------------ */
 

@@ -49,6 +49,14 @@ int ora_decode_step(ora_model *m, const int32_t *tokens, int B, double tau, cons
                     const int32_t *tf_exit, const int32_t *tf_ids, int32_t *next_ids, int32_t *exit_layer,
                     double *dbg_hidden, double *dbg_s, double *dbg_logits, int32_t *n_forced);
 
+/* One decoder layer (1-based `layer`) for rows 0..B-1 at their current
+ * positions len[b] (len is not advanced): river[b] selects the river copy.
+ * Writes the rows' K/V slot of that layer.  h_in, h_out: [B][d]. */
+int ora_layer_forward(ora_model *m, int layer, int B, const int32_t *river, const double *h_in, double *h_out);
+
+/* Final RMSNorm + original LM head + greedy pick for rows 0..B-1 (h: [B][d]). */
+int ora_head(ora_model *m, int B, const double *h, double *logits, int32_t *ids);
+
 int ora_kv_reset(ora_model *m, const int32_t *rows, int n_rows);
 int ora_get_kv(const ora_model *m, uint16_t *dst, size_t bytes);
 int ora_set_kv(ora_model *m, const uint16_t *src, size_t bytes, const int32_t *lens);

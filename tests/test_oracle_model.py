@@ -322,3 +322,26 @@ def test_teacher_forcing_on_ties(tiny_weights):
     assert tf["exit_layer"][0] in (other, free["exit_layer"][0])
     assert tf["n_forced"][0] >= (1 if tf["exit_layer"][0] != free["exit_layer"][0] else 0)
     m.close()
+
+
+def test_layer_forward_and_head_compose_to_decode_step(tiny_weights):
+    """Chaining the single-layer entry point over layers 1..L from the same
+    cache state reproduces a decode step exactly, and the head reproduces its
+    logits and greedy id."""
+    B = 2
+    m = oracle.Model(TINY, tiny_weights, B, 16)
+    m.quantize_river(64)
+    m.prefill(synth.make_prompt(TINY.vocab, B, 5, seed=21), 2.0, fixed_exit=1)
+    kv, lens = m.get_kv(), m.lens()
+    forced = [0, 2]
+    ref = m.decode_step([7, 8], 2.0, forced=forced, debug=True)
+    m.set_kv(kv, lens)
+    h = ref["hidden"][0].copy()
+    for l in range(1, TINY.n_layers + 1):
+        river = [1 if forced[b] < l else 0 for b in range(B)]
+        h = m.layer_forward(l, h, river)
+        assert np.array_equal(h, ref["hidden"][l])
+    logits, ids = m.head(h)
+    assert np.array_equal(logits, ref["logits"]) and np.array_equal(ids, ref["next_ids"])
+    assert list(m.lens()) == list(lens)  # positions not advanced
+    m.close()
