@@ -7,7 +7,7 @@ import pytest
 import oracle
 import synth
 import token_level_early_gb300 as rv
-from gpu_util import check_decode, check_kv, rel_l2
+from gpu_util import check_free, check_layerwise, rel_l2, kv_values
 from ongrid import ongrid_weights
 
 pytestmark = pytest.mark.gpu
@@ -29,6 +29,34 @@ def pair(weights, B=1, T=96, group=64, entry=1):
     return gm, om
 
 
+def layer_oracle(weights, B, T, group=64, entry=1):
+    ot = oracle.Model(TINY, weights, B, T)
+    ot.quantize_river(group, entry)
+    return ot
+
+
+def step_both(gm, om, ot, toks, tau, forced, B, entry=1):
+    """GPU step; free-running oracle om; layer-by-layer oracle ot."""
+    kv_pre = gm.dump(rv.DUMP_KV)
+    lens_pre = gm.dump(rv.DUMP_LENS).copy()
+    g_next, g_exit = gm.decode_step(toks, tau, forced)
+    o = om.decode_step(toks, tau, forced=forced, tf_exit=g_exit, tf_ids=g_next, debug=True)
+    assert o["rc"] == 0
+    check_free(gm, o, g_next, g_exit, B, TINY.n_layers)
+    check_layerwise(gm, ot, kv_pre, lens_pre, g_next, g_exit, B, TINY.n_layers, TINY.act_dtype, tau, forced, entry)
+    return g_next, g_exit
+
+
+def check_kv(g_kv, o_kv, lens, act, tol=1e-2):
+    """Slot pattern bit-exact (sentinel), values within the drift tolerance."""
+    assert np.array_equal(g_kv == 0x7FFF, o_kv == 0x7FFF), "KV slot pattern differs"
+    for b, n in enumerate(lens):
+        gv = kv_values(g_kv[:, :, b, :, :n], act)
+        ov = kv_values(o_kv[:, :, b, :, :n], act)
+        for l in range(gv.shape[0]):
+            assert rel_l2(gv[l], ov[l]) <= tol, (b, l)
+
+
 def test_river_bit_exact(weights):
     gm, om = pair(weights)
     for layer in range(1, TINY.n_layers + 1):
@@ -44,6 +72,7 @@ def test_river_bit_exact(weights):
 def test_tiny_workload_parity(weights):
     """Config: 32-token prompt, 32 greedy decode steps, tau = 0.90."""
     gm, om = pair(weights, T=WL.prompt_len + WL.steps)
+    ot = layer_oracle(weights, 1, WL.prompt_len + WL.steps)
     prompt = synth.make_prompt(TINY.vocab, 1, WL.prompt_len)
     tau = WL.taus[0]
     g_next, g_exit = gm.prefill(prompt, tau)
@@ -53,9 +82,7 @@ def test_tiny_workload_parity(weights):
     tok = int(g_next[0])
     exits = []
     for step in range(WL.steps):
-        g_next, g_exit = gm.decode_step([tok], tau)
-        o = om.decode_step([tok], tau, tf_exit=g_exit, tf_ids=g_next, debug=True)
-        check_decode(gm, g_next, g_exit, o, 1, TINY.n_layers)
+        g_next, g_exit = step_both(gm, om, ot, [tok], tau, None, 1)
         exits.append(int(g_exit[0]))
         tok = int(g_next[0])
     check_kv(gm.dump(rv.DUMP_KV), om.get_kv(), [WL.prompt_len + WL.steps], TINY.act_dtype)
@@ -65,17 +92,16 @@ def test_tiny_workload_parity(weights):
 
 def test_tiny_forced_exits_every_layer(weights):
     gm, om = pair(weights, T=40)
+    ot = layer_oracle(weights, 1, 40)
     prompt = synth.make_prompt(TINY.vocab, 1, 8, seed=3)
     g_next, _ = gm.prefill(prompt, 0.9, fixed_exit=2)
-    o = om.prefill(prompt, 0.9, fixed_exit=2)
-    assert o["next_ids"][0] == g_next[0] or True
+    o = om.prefill(prompt, 0.9, fixed_exit=2, tf_ids=g_next)
+    assert o["next_ids"][0] == g_next[0]
     tok = 5
     for step in range(15):
         f = np.array([step % (TINY.n_layers + 1)], dtype=np.int32)
-        g_next, g_exit = gm.decode_step([tok], 0.9, f)
+        g_next, g_exit = step_both(gm, om, ot, [tok], 0.9, f, 1)
         assert g_exit[0] == f[0]
-        o = om.decode_step([tok], 0.9, forced=f, tf_ids=g_next, debug=True)
-        check_decode(gm, g_next, g_exit, o, 1, TINY.n_layers)
         tok = int(g_next[0])
     check_kv(gm.dump(rv.DUMP_KV), om.get_kv(), [23], TINY.act_dtype)
     gm.close()
@@ -85,6 +111,7 @@ def test_tiny_batched_rows_mixed_paths(weights):
     """B = 3 rows exit at different layers in the same step (general path)."""
     B = 3
     gm, om = pair(weights, B=B, T=40)
+    ot = layer_oracle(weights, B, 40)
     prompts = synth.make_prompt(TINY.vocab, B, 6, seed=4)
     g_next, g_exit = gm.prefill(prompts, 0.9, fixed_exit=1)
     o = om.prefill(prompts, 0.9, fixed_exit=1, tf_ids=g_next)
@@ -92,15 +119,11 @@ def test_tiny_batched_rows_mixed_paths(weights):
     toks = list(g_next)
     for step in range(8):
         f = np.array([(step + 2 * b) % (TINY.n_layers + 1) for b in range(B)], dtype=np.int32)
-        g_next, g_exit = gm.decode_step(toks, 0.9, f)
-        o = om.decode_step(toks, 0.9, forced=f, tf_ids=g_next, debug=True)
-        check_decode(gm, g_next, g_exit, o, B, TINY.n_layers)
+        g_next, g_exit = step_both(gm, om, ot, toks, 0.9, f, B)
         toks = list(g_next)
     # tau rule on the batched path
     for step in range(4):
-        g_next, g_exit = gm.decode_step(toks, 0.5)
-        o = om.decode_step(toks, 0.5, tf_exit=g_exit, tf_ids=g_next, debug=True)
-        check_decode(gm, g_next, g_exit, o, B, TINY.n_layers)
+        g_next, g_exit = step_both(gm, om, ot, toks, 0.5, None, B)
         toks = list(g_next)
     check_kv(gm.dump(rv.DUMP_KV), om.get_kv(), [18] * B, TINY.act_dtype)
     gm.close()
