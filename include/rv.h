@@ -153,6 +153,20 @@ int rv_set_debug(rv_model *m, int enable);
  * the buffer's size for max_batch rows (hidden, s, logits use B = max_batch). */
 int rv_debug_dump(rv_model *m, int what, void *dst, size_t bytes);
 
+/* Kernel timing for roofline reports: launch one batch-1 GEMV kernel of the
+ * decode step `iters` times back to back on the model's stream (outside the
+ * step graph) and return its mean device time per launch in *ms_per_launch
+ * (CUDA events) and its algorithmic HBM bytes per launch in *bytes (weights,
+ * the activation vector read, the outputs written).
+ * kind: RV_TIME_GATEUP (RMSNorm + gate/up + SwiGLU of `layer`), RV_TIME_O
+ * (O projection + residual), RV_TIME_LMHEAD (final norm + LM head + argmax).
+ * river selects the int4 copy (gate/up, O).  Leaves the KV cache and the
+ * cached positions untouched; the step's activation buffers are overwritten. */
+#define RV_TIME_GATEUP 0
+#define RV_TIME_O 1
+#define RV_TIME_LMHEAD 2
+int rv_time_kernel(rv_model *m, int kind, int layer, int river, int iters, float *ms_per_launch, double *bytes);
+
 /* Sizes, for callers that allocate dump buffers. */
 size_t rv_kv_bytes(const rv_model *m);
 size_t rv_param_bytes(const rv_model *m, int which /* 0 backbone, 1 river */);

@@ -92,6 +92,9 @@ class ModelShape:
 TINY = ModelShape("tiny", 4, 256, 4, 2, 64, 688, 1024, 0, FP16, 1e-5, 10000.0)
 LLAMA_1B = ModelShape("llama3.2-1b-shape", 16, 2048, 32, 8, 64, 8192, 128256, 1, BF16, 1e-5, 500000.0)
 LLAMA_8B = ModelShape("llama3.1-8b-shape", 32, 4096, 32, 8, 128, 14336, 128256, 0, BF16, 1e-5, 500000.0)
+# Two layers of the 8B shape with a 32000-entry vocab: a ~1.4 GB case whose
+# per-layer matrices are still larger than L2, for profiler captures.
+LAYER8B = ModelShape("llama3.1-8b-shape-2layer", 2, 4096, 32, 8, 128, 14336, 32000, 0, BF16, 1e-5, 500000.0)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -115,6 +118,7 @@ WORKLOADS = {
     "llama8b": Workload("llama8b", LLAMA_8B, 128, 1, 1024, 512, (0.90,), True, 0.90),
     "batch64": Workload("batch64", LLAMA_1B, 128, 64, 256, 128, (), True, 0.90),
     "long64k": Workload("long64k", LLAMA_8B, 128, 1, 65536, 256, (0.90,), False, 0.90, 20),
+    "layer8b": Workload("layer8b", LAYER8B, 128, 1, 64, 16, (0.90,), True, 0.90),
 }
 
 SEED_WEIGHTS = 1234

@@ -28,7 +28,8 @@ PROJ_Q, PROJ_K, PROJ_V, PROJ_O, PROJ_GATE, PROJ_UP, PROJ_DOWN = range(7)
 DUMP_HIDDEN, DUMP_S, DUMP_LOGITS, DUMP_KV, DUMP_LENS = range(5)
 EXPORTED = ("rv_last_error", "rv_load_model", "rv_quantize_river", "rv_export_river", "rv_prefill",
             "rv_decode_step", "rv_decode_step_dev", "rv_sync_status", "rv_kv_reset", "rv_set_debug",
-            "rv_debug_dump", "rv_kv_bytes", "rv_param_bytes", "rv_free_model")
+            "rv_debug_dump", "rv_kv_bytes", "rv_param_bytes", "rv_free_model", "rv_time_kernel")
+TIME_GATEUP, TIME_O, TIME_LMHEAD = 0, 1, 2
 
 
 def nvcc() -> str:
@@ -113,6 +114,8 @@ def lib():
         "rv_kv_bytes": ([vp], sz),
         "rv_param_bytes": ([vp, i32], sz),
         "rv_free_model": ([vp], None),
+        "rv_time_kernel": ([vp, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_float),
+                            ctypes.POINTER(ctypes.c_double)], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -235,6 +238,14 @@ class Model:
             raise ValueError(what)
         _check(lib().rv_debug_dump(self._h, what, _p(a), a.nbytes))
         return a
+
+    def time_kernel(self, kind: int, layer: int, river: bool, iters: int):
+        """Mean device ms per launch and algorithmic bytes per launch of one GEMV kernel."""
+        ms = ctypes.c_float(0)
+        by = ctypes.c_double(0)
+        _check(lib().rv_time_kernel(self._h, kind, layer, 1 if river else 0, iters, ctypes.byref(ms),
+                                    ctypes.byref(by)))
+        return float(ms.value), float(by.value)
 
     def kv_bytes(self) -> int:
         return int(lib().rv_kv_bytes(self._h))

@@ -48,7 +48,7 @@ enum { MAT_QKV = 0, MAT_O = 1, MAT_GU = 2, MAT_D = 3, N_MAT = 4 };
 
 struct RiverDev {
   uint32_t *q = nullptr;
-  __half *s = nullptr, *z = nullptr;
+  __half2 *sz = nullptr;
   int Kp = 0, G = 0;
 };
 
@@ -184,8 +184,7 @@ Mat make_mat(const rv_model *m, const LayerDev &ly, int which) {
   }
   if (m->has_river) {
     mt.r.q = ly.r[which].q;
-    mt.r.s = ly.r[which].s;
-    mt.r.z = ly.r[which].z;
+    mt.r.sz = ly.r[which].sz;
     mt.r.Kp = ly.r[which].Kp;
     mt.r.G = ly.r[which].G;
     mt.r.g = m->group;
@@ -193,11 +192,9 @@ Mat make_mat(const rv_model *m, const LayerDev &ly, int which) {
   return mt;
 }
 
-int gemv_grid(const rv_model *m, int units) {
-  int g = (units + 7) / 8;
-  const int cap = 4 * m->n_sm;
-  return g < cap ? g : cap;
-}
+// Upper bound on a batch-1 GEMV grid: the reduction scratch holds 4 blocks
+// per SM (the launcher also caps the grid at one resident wave).
+int gemv_grid(const rv_model *m, int) { return 4 * m->n_sm; }
 
 // -------------------------------------------------------------- batch-1 step
 
@@ -604,9 +601,8 @@ int rv_quantize_river(rv_model *m, int group_size, int entry_layer) {
       r.G = (mt.K + group_size - 1) / group_size;
       auto &A = m->river_allocs;
       RV_ALLOC(A, r.q, sizeof(uint32_t) * (size_t)mt.N * (r.Kp / 8));
-      RV_ALLOC(A, r.s, sizeof(__half) * (size_t)mt.N * r.G);
-      RV_ALLOC(A, r.z, sizeof(__half) * (size_t)mt.N * r.G);
-      RV_CK(launch_rtn_quantize(mt.w, mt.N, mt.K, m->act, group_size, r.Kp, r.q, r.s, r.z, m->st.err, m->stream));
+      RV_ALLOC(A, r.sz, sizeof(__half2) * (size_t)mt.N * r.G);
+      RV_CK(launch_rtn_quantize(mt.w, mt.N, mt.K, m->act, group_size, r.Kp, r.q, r.sz, m->st.err, m->stream));
     }
   }
   int32_t err = 0;
@@ -640,8 +636,13 @@ int rv_export_river(const rv_model *m, int layer, int proj, void *q_packed, void
   if (q_packed)
     RV_CK(cudaMemcpy2D(q_packed, sizeof(uint32_t) * (K / 8), r.q + (size_t)row0 * (r.Kp / 8), sizeof(uint32_t) * (r.Kp / 8),
                        sizeof(uint32_t) * (K / 8), rows, cudaMemcpyDeviceToHost));
-  if (scales) RV_CK(cudaMemcpy(scales, r.s + (size_t)row0 * r.G, sizeof(__half) * (size_t)rows * r.G, cudaMemcpyDeviceToHost));
-  if (zeros) RV_CK(cudaMemcpy(zeros, r.z + (size_t)row0 * r.G, sizeof(__half) * (size_t)rows * r.G, cudaMemcpyDeviceToHost));
+  // (scale, zero) pairs are interleaved on the device: pick each half with a pitched copy
+  const __half *sz0 = reinterpret_cast<const __half *>(r.sz + (size_t)row0 * r.G);
+  const size_t n_sz = (size_t)rows * r.G;
+  if (scales)
+    RV_CK(cudaMemcpy2D(scales, sizeof(__half), sz0, sizeof(__half2), sizeof(__half), n_sz, cudaMemcpyDeviceToHost));
+  if (zeros)
+    RV_CK(cudaMemcpy2D(zeros, sizeof(__half), sz0 + 1, sizeof(__half2), sizeof(__half), n_sz, cudaMemcpyDeviceToHost));
   return RV_OK;
 }
 
@@ -836,6 +837,69 @@ int rv_debug_dump(rv_model *m, int what, void *dst, size_t bytes) {
   if (!src) return fail(RV_ESTATE, "debug buffers not enabled (rv_set_debug)");
   if (bytes != need) return fail(RV_EINVAL, "size mismatch: need %zu bytes", need);
   RV_CK(cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost));
+  return RV_OK;
+}
+
+int rv_time_kernel(rv_model *m, int kind, int layer, int river, int iters, float *ms_per_launch, double *bytes) {
+  g_err.clear();
+  if (check_common(m)) return RV_EINVAL;
+  if (!ms_per_launch || !bytes || iters < 1 || kind < 0 || kind > 2) return fail(RV_EINVAL, "bad argument");
+  if (layer < 1 || layer > m->L) return fail(RV_EINVAL, "layer out of range");
+  if (river && (!m->has_river || kind == RV_TIME_LMHEAD)) return fail(RV_ESTATE, "no river copy for this kernel");
+  cudaStream_t s = m->stream;
+  RV_CK(cudaStreamSynchronize(s));
+  const int32_t route = river ? 1 : 0;
+  RV_CK(cudaMemcpy(m->st.route, &route, sizeof(int32_t), cudaMemcpyHostToDevice));
+  const LayerDev &ly = m->layers[layer - 1];
+  GemvArgs a{};
+  a.st = m->st;
+  a.kv = m->kv;
+  a.layer = layer - 1;
+  a.L = m->L; a.H = m->H; a.Hkv = m->Hkv; a.hd = m->hd;
+  a.eps = m->c.rms_eps;
+  a.rope_cs = m->rope_cs;
+  a.partials = m->partials;
+  int pro, epi;
+  if (kind == RV_TIME_GATEUP) {
+    a.m = make_mat(m, ly, MAT_GU);
+    a.h = m->hbuf[0]; a.gamma = ly.mlp_norm; a.out_vec = m->abuf;
+    pro = PRO_NORM; epi = EPI_SWIGLU;
+  } else if (kind == RV_TIME_O) {
+    a.m = make_mat(m, ly, MAT_O);
+    a.vec = m->obuf; a.h_base = m->hbuf[0]; a.h_out = m->hmid;
+    pro = PRO_VEC; epi = EPI_RESID;
+  } else {
+    a.m.w = m->lm_head; a.m.N = m->V; a.m.K = m->d;
+    a.h = m->hbuf[0]; a.gamma = m->final_norm;
+    a.counter = m->counters + m->L + 1;
+    pro = PRO_NORM; epi = EPI_LOGITS;
+  }
+  const double N = a.m.N, K = a.m.K;
+  double wbytes;
+  if (river) {
+    const int G = (a.m.K + m->group - 1) / m->group;
+    wbytes = N * (K / 2.0) + N * G * 4.0;
+  } else {
+    wbytes = N * K * 2.0;
+  }
+  // weights + the activation vector read + one fp32 output per row written
+  const double out_rows = epi == EPI_SWIGLU ? N / 2 : (epi == EPI_LOGITS ? 0 : N);
+  *bytes = wbytes + K * 4.0 + out_rows * 4.0;
+  cudaEvent_t e0, e1;
+  RV_CK(cudaEventCreate(&e0));
+  RV_CK(cudaEventCreate(&e1));
+  RV_CK(launch_gemv_b1(m->act, pro, epi, a, gemv_grid(m, 0), s));  // warm launch
+  RV_CK(cudaEventRecord(e0, s));
+  for (int i = 0; i < iters; ++i) RV_CK(launch_gemv_b1(m->act, pro, epi, a, gemv_grid(m, 0), s));
+  RV_CK(cudaEventRecord(e1, s));
+  RV_CK(cudaEventSynchronize(e1));
+  float ms = 0.f;
+  RV_CK(cudaEventElapsedTime(&ms, e0, e1));
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  *ms_per_launch = ms / iters;
+  // the LM head's argmax advanced len[0]; restore the host's view
+  RV_CK(cudaMemcpy(m->st.len, m->h_len.data(), sizeof(int32_t) * m->Bmax, cudaMemcpyHostToDevice));
   return RV_OK;
 }
 

@@ -56,11 +56,10 @@ __device__ __forceinline__ float block_sum(float v, float *scratch) {
 
 // River copy of one projection in the device layout: canonical packing with
 // the row stride padded to Kp (a multiple of 32) nibbles; fp16 scale and zero
-// per (row, group of g columns).
+// per (row, group of g columns), interleaved as one half2 (scale, zero).
 struct RiverMat {
-  const uint32_t *q;  // [N][Kp/8]
-  const __half *s;    // [N][G]
-  const __half *z;    // [N][G]
+  const uint32_t *q;   // [N][Kp/8]
+  const __half2 *sz;   // [N][G]
   int Kp, G, g;
 };
 

@@ -11,7 +11,7 @@ enum { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_DOWN = 3, EPI_LOGITS = 4 
 // Arguments of the batch-1 GEMV kernels (see decode_b1.cu).
 struct GemvArgs {
   Mat m;
-  int units;  // output rows (or row pairs) to produce
+  int units;  // unused: the launcher derives the work from the matrix and epilogue
   // prologue
   const float *h;         // PRO_NORM: residual stream [K]
   const uint16_t *gamma;  // PRO_NORM: RMSNorm gain [K]
@@ -120,8 +120,8 @@ cudaError_t launch_copy_rows(const float *src, int src_stride, float *dst, int d
                              cudaStream_t s);
 
 // ---------------------------------------------------------------- river construction
-cudaError_t launch_rtn_quantize(const uint16_t *W, int N, int K, int act, int g, int Kp, uint32_t *q, __half *sc,
-                                __half *zp, int32_t *err, cudaStream_t s);
+cudaError_t launch_rtn_quantize(const uint16_t *W, int N, int K, int act, int g, int Kp, uint32_t *q, __half2 *sz,
+                                int32_t *err, cudaStream_t s);
 cudaError_t launch_rope_table(float2 *cs, int T, int hd, double theta, cudaStream_t s);
 cudaError_t launch_fill_u16(uint16_t *p, size_t n, uint16_t v, cudaStream_t s);
 

@@ -9,7 +9,8 @@
 //   z = clamp(rint(-min / s), 0, 15)
 //   q = clamp(rint(w / s) + z, 0, 15)  (rint: half to even)
 // Codes are packed 8 per uint32, element k of a row in bits 4*(k%8) of word
-// k/8, each row padded to Kp (a multiple of 32) with zero codes.
+// k/8, each row padded to Kp (a multiple of 32) with zero codes; scale and
+// zero of a group are stored side by side as one half2.
 #include <math.h>
 
 #include "common.cuh"
@@ -17,7 +18,7 @@
 
 namespace rv {
 
-__global__ void k_rtn(const uint16_t *W, int N, int K, int act, int g, int Kp, uint32_t *q, __half *sc, __half *zp,
+__global__ void k_rtn(const uint16_t *W, int N, int K, int act, int g, int Kp, uint32_t *q, __half2 *sz,
                       int32_t *err) {
   const int G = (K + g - 1) / g, words = Kp >> 3;
   const long total = (long)N * G;
@@ -58,16 +59,15 @@ __global__ void k_rtn(const uint16_t *W, int N, int K, int act, int g, int Kp, u
       }
       q[(size_t)n * words + (kb >> 3)] = word;
     }
-    sc[(size_t)n * G + gi] = s16;
-    zp[(size_t)n * G + gi] = __float2half_rn(z);
+    sz[(size_t)n * G + gi] = __halves2half2(s16, __float2half_rn(z));
   }
 }
 
-cudaError_t launch_rtn_quantize(const uint16_t *W, int N, int K, int act, int g, int Kp, uint32_t *q, __half *sc,
-                                __half *zp, int32_t *err, cudaStream_t s) {
+cudaError_t launch_rtn_quantize(const uint16_t *W, int N, int K, int act, int g, int Kp, uint32_t *q, __half2 *sz,
+                                int32_t *err, cudaStream_t s) {
   const long total = (long)N * ((K + g - 1) / g);
   const int grid = (int)((total + 255) / 256 < 65536 ? (total + 255) / 256 : 65536);
-  k_rtn<<<grid, 256, 0, s>>>(W, N, K, act, g, Kp, q, sc, zp, err);
+  k_rtn<<<grid, 256, 0, s>>>(W, N, K, act, g, Kp, q, sz, err);
   return cudaGetLastError();
 }
 
