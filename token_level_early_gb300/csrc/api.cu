@@ -5,7 +5,9 @@
 // steps (token-level exit) on the model's stream.  Decode steps are captured
 // once per batch size in a CUDA graph: every per-step value (tokens, tau,
 // forced exits, positions, routes) lives in device memory, so a step is one
-// host-to-device copy, one graph launch and one device-to-host copy.
+// host-to-device copy, one graph launch and one device-to-host copy.  The
+// batch-1 chain is launched with programmatic dependent launch, so each
+// kernel's launch and weight prefetch overlap its predecessor's tail.
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -203,7 +205,7 @@ int enqueue_step_b1(rv_model *m, cudaStream_t s) {
   RV_CK(cudaMemsetAsync(m->st.err, 0, sizeof(int32_t), s));
   RV_CK(launch_step_init(m->st, 1, L, s));
   RV_CK(launch_embed(m->embed, m->d, m->act, m->st.tokens, 1, m->V, m->hbuf[0], m->debug ? m->dbg_h : nullptr,
-                     m->st.err, s));
+                     m->st.err, s, 1));
   for (int l = 0; l < L; ++l) {
     const LayerDev &ly = m->layers[l];
     float *hin = m->hbuf[l & 1], *hout = m->hbuf[(l + 1) & 1];
@@ -220,25 +222,25 @@ int enqueue_step_b1(rv_model *m, cudaStream_t s) {
     a.m = make_mat(m, ly, MAT_QKV);
     a.units = m->qkv_n / 2;
     a.h = hin; a.gamma = ly.attn_norm; a.out_vec = m->qbuf;
-    RV_CK(launch_gemv_b1(m->act, PRO_NORM, EPI_QKV, a, gemv_grid(m, a.units), s));
+    RV_CK(launch_gemv_b1(m->act, PRO_NORM, EPI_QKV, a, gemv_grid(m, a.units), s, 1));
 
     AttnArgs at{};
     at.kv = m->kv; at.layer = l; at.H = m->H; at.Hkv = m->Hkv; at.hd = m->hd; at.act = m->act;
     at.q = m->qbuf; at.o = m->obuf; at.len = m->st.len; at.splits = m->attn_splits_b1;
     at.part = m->attn_part; at.counter = m->attn_counter;
-    RV_CK(launch_attn_decode(at, 1, s));
+    RV_CK(launch_attn_decode(at, 1, s, 1));
 
     // O projection + residual
     a.m = make_mat(m, ly, MAT_O);
     a.units = m->d;
     a.vec = m->obuf; a.h_base = hin; a.h_out = m->hmid;
-    RV_CK(launch_gemv_b1(m->act, PRO_VEC, EPI_RESID, a, gemv_grid(m, a.units), s));
+    RV_CK(launch_gemv_b1(m->act, PRO_VEC, EPI_RESID, a, gemv_grid(m, a.units), s, 1));
 
     // MLP in: RMSNorm -> gate/up -> SwiGLU
     a.m = make_mat(m, ly, MAT_GU);
     a.units = m->F;
     a.h = m->hmid; a.gamma = ly.mlp_norm; a.out_vec = m->abuf;
-    RV_CK(launch_gemv_b1(m->act, PRO_NORM, EPI_SWIGLU, a, gemv_grid(m, a.units), s));
+    RV_CK(launch_gemv_b1(m->act, PRO_NORM, EPI_SWIGLU, a, gemv_grid(m, a.units), s, 1));
 
     // down projection + residual + s(l) + exit decision
     a.m = make_mat(m, ly, MAT_D);
@@ -247,7 +249,7 @@ int enqueue_step_b1(rv_model *m, cudaStream_t s) {
     a.counter = m->counters + l;
     a.dbg_h = m->debug ? m->dbg_h + (size_t)(l + 1) * B * m->d : nullptr;
     a.dbg_s = m->debug ? m->dbg_s + (size_t)l * B : nullptr;
-    RV_CK(launch_gemv_b1(m->act, PRO_VEC, EPI_DOWN, a, gemv_grid(m, a.units), s));
+    RV_CK(launch_gemv_b1(m->act, PRO_VEC, EPI_DOWN, a, gemv_grid(m, a.units), s, 1));
   }
   // final RMSNorm + LM head + greedy argmax
   GemvArgs a{};
@@ -258,7 +260,7 @@ int enqueue_step_b1(rv_model *m, cudaStream_t s) {
   a.partials = m->partials;
   a.counter = m->counters + L;
   a.dbg_logits = m->debug ? m->dbg_logits : nullptr;
-  RV_CK(launch_gemv_b1(m->act, PRO_NORM, EPI_LOGITS, a, gemv_grid(m, a.units), s));
+  RV_CK(launch_gemv_b1(m->act, PRO_NORM, EPI_LOGITS, a, gemv_grid(m, a.units), s, 1));
   return RV_OK;
 }
 

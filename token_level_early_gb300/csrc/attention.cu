@@ -20,6 +20,8 @@ constexpr int TILE = 32;
 
 template <int HD, int GRP>
 __global__ void __launch_bounds__(GRP * 32) k_attn(AttnArgs a, int T_per_row, const int32_t *base, int rows) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x, sp = blockIdx.y, g = blockIdx.z;
   if (m >= rows) return;
   const int b = m / T_per_row;
@@ -127,16 +129,17 @@ __global__ void __launch_bounds__(GRP * 32) k_attn(AttnArgs a, int T_per_row, co
 }
 
 template <int HD, int GRP>
-static cudaError_t launch_hg(const AttnArgs &a, int T_per_row, const int32_t *base, int rows, cudaStream_t s) {
+static cudaError_t launch_hg(const AttnArgs &a, int T_per_row, const int32_t *base, int rows, cudaStream_t s,
+                             int pdl) {
   dim3 grid(rows, a.splits, a.Hkv);
-  k_attn<HD, GRP><<<grid, GRP * 32, 0, s>>>(a, T_per_row, base, rows);
-  return cudaGetLastError();
+  return launch_k(k_attn<HD, GRP>, grid, dim3(GRP * 32), 0, s, pdl, a, T_per_row, base, rows);
 }
 
-static cudaError_t launch_any(const AttnArgs &a, int T_per_row, const int32_t *base, int rows, cudaStream_t s) {
+static cudaError_t launch_any(const AttnArgs &a, int T_per_row, const int32_t *base, int rows, cudaStream_t s,
+                              int pdl = 0) {
   const int grp = a.H / a.Hkv;
 #define RV_ATT(HD_, G_) \
-  if (a.hd == HD_ && grp == G_) return launch_hg<HD_, G_>(a, T_per_row, base, rows, s);
+  if (a.hd == HD_ && grp == G_) return launch_hg<HD_, G_>(a, T_per_row, base, rows, s, pdl);
   RV_ATT(64, 1) RV_ATT(64, 2) RV_ATT(64, 4) RV_ATT(64, 8)
   RV_ATT(128, 1) RV_ATT(128, 2) RV_ATT(128, 4) RV_ATT(128, 8)
 #undef RV_ATT
@@ -144,7 +147,9 @@ static cudaError_t launch_any(const AttnArgs &a, int T_per_row, const int32_t *b
 }
 
 // Decode: one row per batch entry, the token at position len[b].
-cudaError_t launch_attn_decode(const AttnArgs &a, int B, cudaStream_t s) { return launch_any(a, 1, a.len, B, s); }
+cudaError_t launch_attn_decode(const AttnArgs &a, int B, cudaStream_t s, int pdl) {
+  return launch_any(a, 1, a.len, B, s, pdl);
+}
 
 // Prefill / general rows: T tokens per sequence starting at base (NULL = 0).
 cudaError_t launch_attn_rows(const AttnRowsArgs &r, int max_rows, cudaStream_t s) {

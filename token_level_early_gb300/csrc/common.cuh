@@ -26,6 +26,34 @@ __device__ __forceinline__ uint16_t f_to_act(float x, int act) {
 
 __device__ __forceinline__ float round_act(float x, int act) { return act_to_f(f_to_act(x, act), act); }
 
+// ------------------------------------------------------------------ launch chaining
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while its predecessor drains;
+// pdl_wait() blocks until the predecessor grid has completed and its writes
+// are visible, pdl_trigger() lets the next kernel in the chain launch.  Both
+// are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with the programmatic stream-serialization attribute when pdl != 0.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int pdl,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, fn, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ reductions
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -11,12 +11,15 @@
 // matrix or its int4 river copy (same kernel, same grid), so a step needs no
 // host round trip per layer and is captured once in a CUDA graph.
 //
-// GEMV engine.  A warp owns 4 output rows (a "quad") and a subset of the K
-// chunks; the 8 warps of a block split K (S ways) and cover 8/S quads.  A
-// lane's activation chunk sits in registers and serves the 4 rows; lanes
-// stream 16-byte weight pieces (a coalesced 512-byte run per row and warp).
-// Partial sums are reduced across lanes by a transpose-reduce and across the
-// K splits through shared memory; the epilogue then runs once per row.
+// GEMV engine.  A warp owns 4 output rows (a "quad") and, when a matrix has
+// too few quads to fill the GPU, one of S splits of its K chunks (S warps of
+// a block per quad).  Weights stream into a per-warp ring of shared-memory
+// stages by cp.async (16-byte pieces, a coalesced 512-byte run per row and
+// stage), NST - 1 work items ahead of the math; the first ones are issued
+// before the kernel waits on its predecessor.  A lane's activation chunk is
+// read from shared memory and serves the 4 rows.  Partial sums are reduced
+// across lanes by a transpose-reduce and, for S > 1, across the splits
+// through shared memory; the epilogue runs in the warp that owns the quad.
 //
 // int4 inner loop.  A code q becomes the float 1 + q/16 (nibble rotated into
 // mantissa bits 19..22 and the exponent of 1.0 OR-ed in) or 1 + q/256 (bits
@@ -112,8 +115,6 @@ __device__ __forceinline__ void quad_rows(const GemvArgs &a, int qd, int *rows) 
   }
 }
 
-__host__ __device__ __forceinline__ int split_of(int nk) { return nk >= 8 ? 8 : nk >= 4 ? 4 : nk >= 2 ? 2 : 1; }
-
 // Transpose-reduce of 4 per-lane values over the warp: the total of v[r]
 // ends in lane 8 * r.
 __device__ __forceinline__ float quad_reduce(const float *v, int lane) {
@@ -159,35 +160,139 @@ __host__ __device__ __forceinline__ Geo geo_of(const Mat &m) {
   return g;
 }
 
-// Shared memory (floats): activations in the lane layout of the larger path,
-// then 256 floats of reduction scratch.
-__host__ __device__ __forceinline__ size_t smem_floats(const Geo &g) {
+// Weight staging: every warp owns a ring of NST stages; a stage holds one
+// work item (one K chunk of the warp's 4 rows: 32 lanes x 16 bytes per row,
+// plus the rows' (scale, zero) words on the int4 path), copied by cp.async.
+constexpr int NST = 4;
+constexpr int STAGE_W = 4 * 32 * 16;
+constexpr int STAGE_S = 4 * 32 * 4;
+constexpr int STAGE = STAGE_W + STAGE_S;
+
+// Shared memory (bytes): activations in the lane layout of the larger path,
+// 256 floats of reduction scratch, then the warps' staging rings.
+__host__ __device__ __forceinline__ size_t x_floats(const Geo &g) {
   const size_t river = (size_t)g.nk4 * (8 * 32 * 4 + 32 * 2);
   const size_t b16 = (size_t)g.nk16 * (2 * 32 * 4);
-  return (river > b16 ? river : b16) + 256;
+  return river > b16 ? river : b16;
+}
+__host__ __device__ __forceinline__ size_t smem_bytes(const Geo &g) {
+  return sizeof(float) * (x_floats(g) + 256) + (size_t)NW * NST * STAGE;
 }
 
+__device__ __forceinline__ void cp16(void *dst, const void *src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp4(void *dst, const void *src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Eight consecutive activations x[k0..k0+8) (k0 a multiple of 8, all < K).
 template <int ACT, int PRO>
-__device__ __forceinline__ float x_at(const GemvArgs &a, int k, float r) {
-  if (PRO == PRO_NORM) return round_act(a.h[k] * r * act_to_f(a.gamma[k], ACT), ACT);
-  return a.vec[k];
+__device__ __forceinline__ void load_x8(const GemvArgs &a, int k0, float r, float *x) {
+  const float4 *src = reinterpret_cast<const float4 *>((PRO == PRO_NORM ? a.h : a.vec) + k0);
+  const float4 u0 = src[0], u1 = src[1];
+  x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+  x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+  if (PRO == PRO_NORM) {
+    const uint4 gw = *reinterpret_cast<const uint4 *>(a.gamma + k0);
+    const uint16_t *gp = reinterpret_cast<const uint16_t *>(&gw);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = round_act(x[j] * r * act_to_f(gp[j], ACT), ACT);
+  }
+}
+
+// K splits per row quad: the smallest power of two (<= 8, <= chunks) that
+// gives at least 4096 (quad, split) tasks, so small matrices still fill the
+// GPU while large ones run without cross-warp reductions.
+__host__ __device__ __forceinline__ int splits_for(int nquads, int nk) {
+  int S = 1;
+  while (S < 8 && 2 * S <= nk && nquads * S < 4096) S *= 2;
+  return S;
+}
+
+// The warp's stream of work items (quad, chunk) in consumption order: quads
+// bq + rg for bq = blockIdx.x * RG, + gridDim.x * RG, ...; chunks sp, sp + S..
+struct ItemStream {
+  int bq, c;
+};
+
+template <int EPI>
+__device__ __forceinline__ void issue_item(const GemvArgs &a, const Geo &g, int river, int rg, int nquads, int nk,
+                                           int S, int sp, int RG, ItemStream &is, char *stage, int lane) {
+  if (is.bq + rg < nquads) {
+    int rows[4];
+    quad_rows<EPI>(a, is.bq + rg, rows);
+    if (river) {
+      const int k0 = is.c * CH4 + lane * 32;
+      if (k0 < g.Kp) {
+        const RiverMat &R = a.m.r;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          cp16(stage + (r * 32 + lane) * 16, R.q + (size_t)rows[r] * g.words + (k0 >> 3));
+          cp4(stage + STAGE_W + (r * 32 + lane) * 4, R.sz + (size_t)rows[r] * g.G + k0 / R.g);
+        }
+      }
+    } else {
+      const int k0 = is.c * CH16 + lane * 8;
+      if (k0 < g.K) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) cp16(stage + (r * 32 + lane) * 16, a.m.w + (size_t)rows[r] * g.K + k0);
+      }
+    }
+    is.c += S;
+    if (is.c >= nk) {
+      is.c = sp;
+      is.bq += gridDim.x * RG;
+    }
+  }
+  cp_commit();  // one group per item slot, empty once the stream has ended
 }
 
 template <int ACT, int PRO, int EPI>
-__global__ void __launch_bounds__(NW * 32, 3) k_gemv_b1(GemvArgs a) {
+__global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
   extern __shared__ __align__(16) float smem[];
   const Geo g = geo_of(a.m);
-  const int river = (EPI == EPI_LOGITS) ? 0 : a.st.route[0];
-  const int nk = river ? g.nk4 : g.nk16;
-  float *red = smem + (smem_floats(g) - 256);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nquads = a.m.N >> 2;
+  float *scratch = smem + x_floats(g);
+  float *red = scratch;        // [2][NW * 4]: cross-warp partials, double-buffered
+  float *bsum = scratch + 64;  // block_sum scratch (3 x 32)
+  char *ring = reinterpret_cast<char *>(scratch + 256) + (size_t)warp * NST * STAGE;
+
+  // In a PDL chain the route flag is final before this kernel starts for
+  // every GEMV but QKV (it was written at least two kernels earlier): those
+  // start streaming their first weight chunks while the predecessor drains.
+  // QKV's route comes from its direct predecessor, so it waits first.
+  int river = 0;
+  if (EPI != EPI_QKV) {
+    river = (EPI == EPI_LOGITS) ? 0 : a.st.route[0];
+  } else {
+    pdl_wait();
+    river = a.st.route[0];
+  }
+  const int nk = river ? g.nk4 : g.nk16;
+  const int S = river ? a.s4 : a.s16, RG = NW / S, rg = warp / S, sp = warp % S;
+  ItemStream is{(int)blockIdx.x * RG, sp};
+#pragma unroll
+  for (int i = 0; i < NST - 1; ++i)
+    issue_item<EPI>(a, g, river, rg, nquads, nk, S, sp, RG, is, ring + i * STAGE, lane);
+  if (EPI != EPI_QKV) pdl_wait();
+  pdl_trigger();
 
   // ---- prologue: x = round16(RMSNorm(h) * gamma) or x = vec, in the lane layout
   float rs = 0.f;
   if (PRO == PRO_NORM) {
     float ss = 0.f;
-    for (int i = tid; i < g.K; i += blockDim.x) ss = fmaf(a.h[i], a.h[i], ss);
-    ss = block_sum(ss, red);
+    for (int i = tid * 4; i < g.K; i += blockDim.x * 4) {
+      const float4 v = *reinterpret_cast<const float4 *>(a.h + i);
+      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+    }
+    ss = block_sum(ss, bsum);
     rs = 1.0f / sqrtf(ss / (float)g.K + a.eps);
   }
   if (river) {
@@ -196,22 +301,17 @@ __global__ void __launch_bounds__(NW * 32, 3) k_gemv_b1(GemvArgs a) {
     for (int t = tid; t < nk * 32; t += blockDim.x) {
       const int c = t >> 5, ln = t & 31, base = c * CH4 + ln * 32;
       float C = 0.f, X = 0.f;
-      const int ev[4] = {0, 2, 4, 6}, od[4] = {7, 1, 3, 5};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        float e[4][2];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int ke = base + 8 * i + ev[p], ko = base + 8 * i + od[p];
-          const float xe = ke < g.K ? x_at<ACT, PRO>(a, ke, rs) : 0.f;
-          const float xo = ko < g.K ? x_at<ACT, PRO>(a, ko, rs) : 0.f;
-          e[p][0] = 16.f * xe;
-          e[p][1] = 256.f * xo;
-          C += e[p][0] + e[p][1];
-          X += xe + xo;
-        }
-        xq[(c * 8 + 2 * i) * 32 + ln] = make_float4(e[0][0], e[0][1], e[1][0], e[1][1]);
-        xq[(c * 8 + 2 * i + 1) * 32 + ln] = make_float4(e[2][0], e[2][1], e[3][0], e[3][1]);
+        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (base + 8 * i < g.K) load_x8<ACT, PRO>(a, base + 8 * i, rs, x);
+        // pairs (even, odd) = (0,7), (2,1), (4,3), (6,5), scaled by 16 and 256
+        const float e0 = 16.f * x[0], o0 = 256.f * x[7], e1 = 16.f * x[2], o1 = 256.f * x[1];
+        const float e2 = 16.f * x[4], o2 = 256.f * x[3], e3 = 16.f * x[6], o3 = 256.f * x[5];
+        xq[(c * 8 + 2 * i) * 32 + ln] = make_float4(e0, o0, e1, o1);
+        xq[(c * 8 + 2 * i + 1) * 32 + ln] = make_float4(e2, o2, e3, o3);
+        C += ((e0 + o0) + (e1 + o1)) + ((e2 + o2) + (e3 + o3));
+        X += ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
       }
       cx[c * 32 + ln] = make_float2(C, X);
     }
@@ -219,43 +319,38 @@ __global__ void __launch_bounds__(NW * 32, 3) k_gemv_b1(GemvArgs a) {
     float4 *xb = reinterpret_cast<float4 *>(smem);  // [nk][2][32]
     for (int t = tid; t < nk * 32; t += blockDim.x) {
       const int c = t >> 5, ln = t & 31, base = c * CH16 + ln * 8;
-      float v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = base + j < g.K ? x_at<ACT, PRO>(a, base + j, rs) : 0.f;
-      xb[(c * 2) * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
-      xb[(c * 2 + 1) * 32 + ln] = make_float4(v[4], v[5], v[6], v[7]);
+      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (base < g.K) load_x8<ACT, PRO>(a, base, rs, x);
+      xb[(c * 2) * 32 + ln] = make_float4(x[0], x[1], x[2], x[3]);
+      xb[(c * 2 + 1) * 32 + ln] = make_float4(x[4], x[5], x[6], x[7]);
     }
   }
   __syncthreads();
 
-  const int S = split_of(nk), RG = NW / S, rg = warp / S, sp = warp % S;
-  const int nquads = a.m.N >> 2;
   const int pos = (EPI == EPI_QKV) ? a.st.len[0] : 0;
   float p_dot = 0.f, p_n1 = 0.f, p_n2 = 0.f;
   float best = -INFINITY;
   int best_i = 0x7fffffff;
+  int parity = 0, t = 0;
 
-  for (int base_q = blockIdx.x * RG; base_q < nquads; base_q += gridDim.x * RG) {
+  for (int base_q = blockIdx.x * RG; base_q < nquads; base_q += gridDim.x * RG, parity ^= 1) {
     const int qd = base_q + rg;
     float v[4] = {0.f, 0.f, 0.f, 0.f};
+    int rows[4] = {0, 0, 0, 0};
     if (qd < nquads) {
-      int rows[4];
       quad_rows<EPI>(a, qd, rows);
-      if (river) {
-        const float4 *xq = reinterpret_cast<const float4 *>(smem);
-        const float2 *cx = reinterpret_cast<const float2 *>(smem + nk * 8 * 32 * 4);
-        const RiverMat &R = a.m.r;
-#pragma unroll 1
-        for (int c = sp; c < nk; c += S) {
+      u64 acc[4] = {0ull, 0ull, 0ull, 0ull};
+      for (int c = sp; c < nk; c += S, ++t) {
+        cp_wait<NST - 2>();  // this lane's copies of item t have landed
+        issue_item<EPI>(a, g, river, rg, nquads, nk, S, sp, RG, is, ring + ((t + NST - 1) % NST) * STAGE, lane);
+        const char *stg = ring + (t % NST) * STAGE;
+        const uint4 *sw = reinterpret_cast<const uint4 *>(stg);
+        if (river) {
           const int k0 = c * CH4 + lane * 32;
           if (k0 >= g.Kp) continue;
-          uint4 w[4];
-          __half2 szh[4];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            w[r] = ld_stream(R.q + (size_t)rows[r] * g.words + (k0 >> 3));
-            szh[r] = R.sz[(size_t)rows[r] * g.G + k0 / R.g];
-          }
+          const float4 *xq = reinterpret_cast<const float4 *>(smem);
+          const float2 cxv = reinterpret_cast<const float2 *>(smem + nk * 8 * 32 * 4)[c * 32 + lane];
+          const __half2 *ss = reinterpret_cast<const __half2 *>(stg + STAGE_W);
           u64 xp[16];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -263,105 +358,103 @@ __global__ void __launch_bounds__(NW * 32, 3) k_gemv_b1(GemvArgs a) {
             xp[2 * i] = pack2(f.x, f.y);
             xp[2 * i + 1] = pack2(f.z, f.w);
           }
-          const float2 cxv = cx[c * 32 + lane];
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
-            u64 acc = 0ull;
-            acc = word_fma(w[r].x, xp + 0, acc);
-            acc = word_fma(w[r].y, xp + 4, acc);
-            acc = word_fma(w[r].z, xp + 8, acc);
-            acc = word_fma(w[r].w, xp + 12, acc);
-            const float2 sz = __half22float2(szh[r]);
-            v[r] = fmaf(sz.x, sum2(acc) - fmaf(sz.y, cxv.y, cxv.x), v[r]);
+            const uint4 w = sw[r * 32 + lane];
+            u64 ac = word_fma(w.x, xp + 0, 0ull);
+            ac = word_fma(w.y, xp + 4, ac);
+            u64 ad = word_fma(w.z, xp + 8, 0ull);
+            ad = word_fma(w.w, xp + 12, ad);
+            const float2 sz = __half22float2(ss[r * 32 + lane]);
+            v[r] = fmaf(sz.x, (sum2(ac) + sum2(ad)) - fmaf(sz.y, cxv.y, cxv.x), v[r]);
           }
-        }
-      } else {
-        const float4 *xb = reinterpret_cast<const float4 *>(smem);
-        u64 acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll 2
-        for (int c = sp; c < nk; c += S) {
+        } else {
           const int k0 = c * CH16 + lane * 8;
           if (k0 >= g.K) continue;
-          uint4 w[4];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) w[r] = ld_stream(a.m.w + (size_t)rows[r] * g.K + k0);
+          const float4 *xb = reinterpret_cast<const float4 *>(smem);
           const float4 f0 = xb[(c * 2) * 32 + lane], f1 = xb[(c * 2 + 1) * 32 + lane];
-          const u64 x0 = pack2(f0.x, f0.y), x1 = pack2(f0.z, f0.w), x2 = pack2(f1.x, f1.y),
-                    x3 = pack2(f1.z, f1.w);
+          const u64 x0 = pack2(f0.x, f0.y), x1 = pack2(f0.z, f0.w), x2 = pack2(f1.x, f1.y), x3 = pack2(f1.z, f1.w);
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
-            acc[r] = pair16_fma<ACT>(w[r].x, x0, acc[r]);
-            acc[r] = pair16_fma<ACT>(w[r].y, x1, acc[r]);
-            acc[r] = pair16_fma<ACT>(w[r].z, x2, acc[r]);
-            acc[r] = pair16_fma<ACT>(w[r].w, x3, acc[r]);
+            const uint4 w = sw[r * 32 + lane];
+            acc[r] = pair16_fma<ACT>(w.x, x0, acc[r]);
+            acc[r] = pair16_fma<ACT>(w.y, x1, acc[r]);
+            acc[r] = pair16_fma<ACT>(w.z, x2, acc[r]);
+            acc[r] = pair16_fma<ACT>(w.w, x3, acc[r]);
           }
         }
+      }
+      if (!river) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) v[r] = sum2(acc[r]);
       }
     }
-    const float m = quad_reduce(v, lane);
-    if ((lane & 7) == 0) red[(rg * S + sp) * 4 + (lane >> 3)] = m;
-    __syncthreads();
-    if (tid < RG * 4) {
-      const int rgt = tid >> 2, r = tid & 3, q2 = base_q + rgt;
-      if (q2 < nquads) {
-        int rows[4];
-        quad_rows<EPI>(a, q2, rows);
-        float y = 0.f;
-        for (int s2 = 0; s2 < S; ++s2) y += red[(rgt * S + s2) * 4 + r];
-        if (EPI == EPI_QKV || EPI == EPI_SWIGLU) {
-          // pairs (0,2) and (1,3): thread r < 2 combines rows r and r + 2
-          if (r < 2) {
-            float y2 = 0.f;
-            for (int s2 = 0; s2 < S; ++s2) y2 += red[(rgt * S + s2) * 4 + r + 2];
-            if (EPI == EPI_SWIGLU) {
-              const float sg = y / (1.0f + expf(-y));
-              a.out_vec[rows[r]] = round_act(sg * y2, ACT);
-            } else {
-              const int half = a.hd >> 1, slot = rows[r] / a.hd, i = rows[r] - slot * a.hd;
-              if (slot < a.H + a.Hkv) {
-                const float2 cs = a.rope_cs[(size_t)pos * half + i];
-                const float o0 = y * cs.x - y2 * cs.y, o1 = y * cs.y + y2 * cs.x;
-                if (slot < a.H) {
-                  a.out_vec[slot * a.hd + i] = round_act(o0, ACT);
-                  a.out_vec[slot * a.hd + i + half] = round_act(o1, ACT);
-                } else {
-                  uint16_t *kp = a.kv.base + a.kv.idx(a.layer, 0, 0, slot - a.H, pos);
-                  kp[i] = f_to_act(o0, ACT);
-                  kp[i + half] = f_to_act(o1, ACT);
-                }
-              } else {
-                uint16_t *vp = a.kv.base + a.kv.idx(a.layer, 1, 0, slot - a.H - a.Hkv, pos);
-                vp[i] = f_to_act(y, ACT);
-                vp[i + half] = f_to_act(y2, ACT);
-              }
-            }
-          }
-        } else if (EPI == EPI_RESID) {
-          a.h_out[rows[r]] = a.h_base[rows[r]] + y;
-        } else if (EPI == EPI_DOWN) {
-          const int u = rows[r];
-          const float hn = a.h_base[u] + y, hi = a.h_in[u];
-          a.h_out[u] = hn;
-          if (a.dbg_h) a.dbg_h[u] = hn;
-          p_dot = fmaf(hi, hn, p_dot);
-          p_n1 = fmaf(hi, hi, p_n1);
-          p_n2 = fmaf(hn, hn, p_n2);
-        } else if (EPI == EPI_LOGITS) {
-          const int u = rows[r];
-          if (a.dbg_logits) a.dbg_logits[u] = y;
-          if (y > best || (y == best && u < best_i)) { best = y; best_i = u; }
-        }
+    // row r of the quad ends in lane 8 r of every warp of the quad's group
+    float m = quad_reduce(v, lane);
+    if (S > 1) {
+      float *rb = red + parity * (NW * 4);
+      if ((lane & 7) == 0) rb[(rg * S + sp) * 4 + (lane >> 3)] = m;
+      __syncthreads();
+      if (sp == 0 && (lane & 7) == 0) {
+        float tt = 0.f;
+        for (int s2 = 0; s2 < S; ++s2) tt += rb[(rg * S + s2) * 4 + (lane >> 3)];
+        m = tt;
       }
     }
-    __syncthreads();
+    if (sp != 0 || qd >= nquads) continue;
+    const int r = lane >> 3;
+    const int row_r = r == 0 ? rows[0] : r == 1 ? rows[1] : r == 2 ? rows[2] : rows[3];
+    // ---- epilogue in the owning warp: lane 8 r holds row r
+    if (EPI == EPI_QKV || EPI == EPI_SWIGLU) {
+      const float y2 = __shfl_down_sync(0xffffffffu, m, 16);  // rows 2, 3 -> lanes 0, 8
+      if ((lane & 7) == 0 && r < 2) {
+        const float y = m;
+        if (EPI == EPI_SWIGLU) {
+          const float sg = y / (1.0f + expf(-y));
+          a.out_vec[row_r] = round_act(sg * y2, ACT);
+        } else {
+          const int half = a.hd >> 1, slot = row_r / a.hd, i = row_r - slot * a.hd;
+          if (slot < a.H + a.Hkv) {
+            const float2 cs = a.rope_cs[(size_t)pos * half + i];
+            const float o0 = y * cs.x - y2 * cs.y, o1 = y * cs.y + y2 * cs.x;
+            if (slot < a.H) {
+              a.out_vec[slot * a.hd + i] = round_act(o0, ACT);
+              a.out_vec[slot * a.hd + i + half] = round_act(o1, ACT);
+            } else {
+              uint16_t *kp = a.kv.base + a.kv.idx(a.layer, 0, 0, slot - a.H, pos);
+              kp[i] = f_to_act(o0, ACT);
+              kp[i + half] = f_to_act(o1, ACT);
+            }
+          } else {
+            uint16_t *vp = a.kv.base + a.kv.idx(a.layer, 1, 0, slot - a.H - a.Hkv, pos);
+            vp[i] = f_to_act(y, ACT);
+            vp[i + half] = f_to_act(y2, ACT);
+          }
+        }
+      }
+    } else if ((lane & 7) == 0) {
+      const int u = row_r;
+      if (EPI == EPI_RESID) {
+        a.h_out[u] = a.h_base[u] + m;
+      } else if (EPI == EPI_DOWN) {
+        const float hn = a.h_base[u] + m, hi = a.h_in[u];
+        a.h_out[u] = hn;
+        if (a.dbg_h) a.dbg_h[u] = hn;
+        p_dot = fmaf(hi, hn, p_dot);
+        p_n1 = fmaf(hi, hi, p_n1);
+        p_n2 = fmaf(hn, hn, p_n2);
+      } else if (EPI == EPI_LOGITS) {
+        if (a.dbg_logits) a.dbg_logits[u] = m;
+        if (m > best || (m == best && u < best_i)) { best = m; best_i = u; }
+      }
+    }
   }
+  cp_wait<0>();  // no copy outlives the kernel
 
   if (EPI == EPI_DOWN) {
-    p_dot = block_sum(p_dot, red);
-    p_n1 = block_sum(p_n1, red + 32);
-    p_n2 = block_sum(p_n2, red + 64);
+    p_dot = block_sum(p_dot, bsum);
+    p_n1 = block_sum(p_n1, bsum + 32);
+    p_n2 = block_sum(p_n2, bsum + 64);
     if (tid == 0) {
       a.partials[blockIdx.x * 3 + 0] = p_dot;
       a.partials[blockIdx.x * 3 + 1] = p_n1;
@@ -374,12 +467,12 @@ __global__ void __launch_bounds__(NW * 32, 3) k_gemv_b1(GemvArgs a) {
       t1 += a.partials[i * 3 + 1];
       t2 += a.partials[i * 3 + 2];
     }
-    t0 = block_sum(t0, red);
-    t1 = block_sum(t1, red + 32);
-    t2 = block_sum(t2, red + 64);
+    t0 = block_sum(t0, bsum);
+    t1 = block_sum(t1, bsum + 32);
+    t2 = block_sum(t2, bsum + 64);
     if (tid == 0) decide_row(a.st, 0, a.layer + 1, a.L, t0, t1, t2, a.dbg_s);
   } else if (EPI == EPI_LOGITS) {
-    // block argmax (lowest index on ties) over the epilogue threads
+    // block argmax (lowest index on ties)
     __shared__ float bv[NW * 32];
     __shared__ int bi[NW * 32];
     bv[tid] = best;
@@ -388,8 +481,8 @@ __global__ void __launch_bounds__(NW * 32, 3) k_gemv_b1(GemvArgs a) {
     if (tid == 0) {
       float vb = bv[0];
       int ib = bi[0];
-      for (int t = 1; t < RG * 4; ++t)
-        if (bv[t] > vb || (bv[t] == vb && bi[t] < ib)) { vb = bv[t]; ib = bi[t]; }
+      for (int q = 1; q < NW * 32; ++q)
+        if (bv[q] > vb || (bv[q] == vb && bi[q] < ib)) { vb = bv[q]; ib = bi[q]; }
       a.partials[blockIdx.x * 2] = vb;
       reinterpret_cast<int *>(a.partials)[blockIdx.x * 2 + 1] = ib;
     }
@@ -411,20 +504,23 @@ __global__ void __launch_bounds__(NW * 32, 3) k_gemv_b1(GemvArgs a) {
 // ------------------------------------------------------------------ launch
 
 template <int ACT, int PRO, int EPI>
-static cudaError_t launch_t(const GemvArgs &a, int max_grid, cudaStream_t s) {
+static cudaError_t launch_t(const GemvArgs &a_in, int max_grid, cudaStream_t s, int pdl) {
+  GemvArgs a = a_in;
   const Geo g = geo_of(a.m);
-  const size_t smem = sizeof(float) * smem_floats(g);
+  const int nq = a.m.N / 4;
+  a.s4 = splits_for(nq, g.nk4);
+  a.s16 = splits_for(nq, g.nk16);
+  const size_t smem = smem_bytes(g);
   auto fn = k_gemv_b1<ACT, PRO, EPI>;
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  // Quad groups per block-iteration depend on the path (the K split
-  // differs): size the grid for the path with more groups, never beyond one
-  // resident wave; the grid-stride loop covers the rest.
-  const int nq = a.m.N / 4;
-  const int nk_max = g.nk4 > g.nk16 ? g.nk4 : g.nk16;
-  const int RG = NW / split_of(nk_max);
+  // Enough blocks for the path with more (quad, split) groups, never beyond
+  // one resident wave; the grid-stride loop covers the rest.
+  const int s_max = a.s4 > a.s16 ? a.s4 : a.s16;
+  const int RG = NW / s_max;
   int grid = (nq + RG - 1) / RG;
   int per_sm = 0, dev = 0, n_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, NW * 32, smem);
@@ -434,15 +530,14 @@ static cudaError_t launch_t(const GemvArgs &a, int max_grid, cudaStream_t s) {
   if (per_sm < 1) per_sm = 1;
   if (grid > per_sm * n_sm) grid = per_sm * n_sm;
   if (grid > max_grid) grid = max_grid;
-  fn<<<grid, NW * 32, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(fn, dim3(grid), dim3(NW * 32), smem, s, pdl, a);
 }
 
-cudaError_t launch_gemv_b1(int act, int pro, int epi, const GemvArgs &a, int max_grid, cudaStream_t s) {
-  if (a.m.N % 4) return cudaErrorInvalidValue;
-#define RV_DISPATCH(PRO_, EPI_)                                                                     \
-  if (pro == PRO_ && epi == EPI_)                                                                   \
-    return act ? launch_t<1, PRO_, EPI_>(a, max_grid, s) : launch_t<0, PRO_, EPI_>(a, max_grid, s);
+cudaError_t launch_gemv_b1(int act, int pro, int epi, const GemvArgs &a, int max_grid, cudaStream_t s, int pdl) {
+  if (a.m.N % 4 || a.m.K % 8) return cudaErrorInvalidValue;
+#define RV_DISPATCH(PRO_, EPI_)                                                                          \
+  if (pro == PRO_ && epi == EPI_)                                                                        \
+    return act ? launch_t<1, PRO_, EPI_>(a, max_grid, s, pdl) : launch_t<0, PRO_, EPI_>(a, max_grid, s, pdl);
   RV_DISPATCH(PRO_NORM, EPI_QKV)
   RV_DISPATCH(PRO_VEC, EPI_RESID)
   RV_DISPATCH(PRO_NORM, EPI_SWIGLU)

@@ -22,6 +22,8 @@ static inline int cdiv(long a, long b) { return (int)((a + b - 1) / b); }
 
 __global__ void k_embed(const uint16_t *E, int d, int act, const int32_t *tokens, int vocab, float *H,
                         float *dbg_h, int32_t *err) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x;
   int tok = tokens[m];
   if (tok < 0 || tok >= vocab) {
@@ -36,10 +38,9 @@ __global__ void k_embed(const uint16_t *E, int d, int act, const int32_t *tokens
 }
 
 cudaError_t launch_embed(const uint16_t *E, int d, int act, const int32_t *tokens, int M, int vocab, float *H,
-                         float *dbg_h, int32_t *err, cudaStream_t s) {
+                         float *dbg_h, int32_t *err, cudaStream_t s, int pdl) {
   if (M <= 0) return cudaSuccess;
-  k_embed<<<M, 256, 0, s>>>(E, d, act, tokens, vocab, H, dbg_h, err);
-  return cudaGetLastError();
+  return launch_k(k_embed, dim3(M), dim3(256), 0, s, pdl, E, d, act, tokens, vocab, H, dbg_h, err);
 }
 
 // Route state at the start of a step (forced mode: exit 0 = all river).

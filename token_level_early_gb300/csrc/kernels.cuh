@@ -11,7 +11,8 @@ enum { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_DOWN = 3, EPI_LOGITS = 4 
 // Arguments of the batch-1 GEMV kernels (see decode_b1.cu).
 struct GemvArgs {
   Mat m;
-  int units;  // unused: the launcher derives the work from the matrix and epilogue
+  int units;   // unused: the launcher derives the work from the matrix and epilogue
+  int s4, s16; // K splits per row quad for the int4 / 16-bit path (set by the launcher)
   // prologue
   const float *h;         // PRO_NORM: residual stream [K]
   const uint16_t *gamma;  // PRO_NORM: RMSNorm gain [K]
@@ -56,7 +57,7 @@ __device__ __forceinline__ void decide_row(const StepState &st, int b, int layer
   }
 }
 
-cudaError_t launch_gemv_b1(int act, int pro, int epi, const GemvArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_gemv_b1(int act, int pro, int epi, const GemvArgs &a, int grid, cudaStream_t s, int pdl = 0);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {
@@ -69,7 +70,7 @@ struct AttnArgs {
   float *part;         // [B][H][splits][hd + 2]
   unsigned *counter;   // [B][Hkv]
 };
-cudaError_t launch_attn_decode(const AttnArgs &a, int B, cudaStream_t s);
+cudaError_t launch_attn_decode(const AttnArgs &a, int B, cudaStream_t s, int pdl = 0);
 
 // Causal attention for token rows of the general path: row m of the list
 // attends to positions 0..pos(m) of its sequence.
@@ -87,7 +88,7 @@ cudaError_t launch_attn_rows(const AttnRowsArgs &a, int max_rows, cudaStream_t s
 
 // ---------------------------------------------------------------- general path
 cudaError_t launch_embed(const uint16_t *E, int d, int act, const int32_t *tokens, int M, int vocab, float *H,
-                         float *dbg_h, int32_t *err, cudaStream_t s);
+                         float *dbg_h, int32_t *err, cudaStream_t s, int pdl = 0);
 cudaError_t launch_step_init(const StepState &st, int B, int L, cudaStream_t s);
 cudaError_t launch_route_lists(const int32_t *route, int B, int T, int32_t *lists, int list_stride,
                                int32_t *counts, cudaStream_t s);
