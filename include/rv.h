@@ -167,6 +167,29 @@ int rv_debug_dump(rv_model *m, int what, void *dst, size_t bytes);
 #define RV_TIME_LMHEAD 2
 int rv_time_kernel(rv_model *m, int kind, int layer, int river, int iters, float *ms_per_launch, double *bytes);
 
+/* Greedy LM head without allocation: final RMSNorm (gain d_final_norm, eps
+ * rms_eps) of the fp32 vector d_h [d_model], the LM-head GEMV against
+ * d_lm_head [vocab][d_model] (16-bit, act_dtype 0 = fp16, 1 = bf16) and the
+ * argmax (lowest index on ties) into d_next_id[0]; d_logits [vocab] (fp32)
+ * receives the logits when not NULL.  All pointers are device pointers; the
+ * call is asynchronous on `stream` (a cudaStream_t, NULL = default stream).
+ * The pages have no counterpart: this entry point exists for callers that
+ * must not allocate device memory (a runtime that owns the whole memory
+ * budget, or code that cannot afford the implicit synchronization of
+ * cudaMalloc/cudaFree).  It runs the decode step's LM-head kernel with its
+ * cross-block scratch (per-block results for at most 1024 blocks, ~8 KB) in
+ * an array compiled into the library, which every GPU that loads the library
+ * holds until the process exits; it calls no allocator.  The first call on a
+ * device looks the array's address up (cudaGetSymbolAddress), so make that
+ * first call before any stream capture.  All calls share the one array:
+ * calls whose executions overlap on the GPU (other streams, other threads)
+ * race and must be serialized by the caller.  Returns RV_EINVAL for
+ * vocab not a positive multiple of 4, d_model not a positive multiple of 8
+ * or d_model above the maximum of 16384. */
+int rv_greedy_head_noalloc(const void *d_lm_head, const void *d_final_norm, const float *d_h, int vocab,
+                           int d_model, int act_dtype, float rms_eps, int32_t *d_next_id, float *d_logits,
+                           void *stream);
+
 /* Sizes, for callers that allocate dump buffers. */
 size_t rv_kv_bytes(const rv_model *m);
 size_t rv_param_bytes(const rv_model *m, int which /* 0 backbone, 1 river */);

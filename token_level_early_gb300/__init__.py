@@ -20,7 +20,7 @@ _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "librv.so")
 _CSRC = os.path.join(_HERE, "csrc")
 _BUILD = os.path.join(_ROOT, "_build")
-SOURCES = ["api.cu", "decode_b1.cu", "attention.cu", "general.cu", "quant.cu"]
+SOURCES = ["api.cu", "decode_b1.cu", "attention.cu", "general.cu", "quant.cu", "noalloc.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 RV_OK, RV_EINVAL, RV_ENOMEM, RV_ECUDA, RV_ECAPACITY, RV_ESTATE, RV_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
@@ -28,7 +28,7 @@ PROJ_Q, PROJ_K, PROJ_V, PROJ_O, PROJ_GATE, PROJ_UP, PROJ_DOWN = range(7)
 DUMP_HIDDEN, DUMP_S, DUMP_LOGITS, DUMP_KV, DUMP_LENS = range(5)
 EXPORTED = ("rv_last_error", "rv_load_model", "rv_quantize_river", "rv_export_river", "rv_prefill",
             "rv_decode_step", "rv_decode_step_dev", "rv_sync_status", "rv_kv_reset", "rv_set_debug",
-            "rv_debug_dump", "rv_kv_bytes", "rv_param_bytes", "rv_free_model", "rv_time_kernel")
+            "rv_debug_dump", "rv_kv_bytes", "rv_param_bytes", "rv_free_model", "rv_time_kernel", "rv_greedy_head_noalloc")
 TIME_GATEUP, TIME_O, TIME_LMHEAD = 0, 1, 2
 
 
@@ -116,6 +116,7 @@ def lib():
         "rv_free_model": ([vp], None),
         "rv_time_kernel": ([vp, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_float),
                             ctypes.POINTER(ctypes.c_double)], i32),
+        "rv_greedy_head_noalloc": ([vp, vp, vp, i32, i32, i32, f32, vp, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -132,6 +133,13 @@ def _check(rc: int):
 
 def _p(a):
     return None if a is None else a.ctypes.data
+
+
+def greedy_head_noalloc(d_lm_head: int, d_final_norm: int, d_h: int, vocab: int, d_model: int, act_dtype: int,
+                        rms_eps: float, d_next_id: int, d_logits: Optional[int] = None, stream: Optional[int] = None):
+    """rv_greedy_head_noalloc on device pointers (see include/rv.h)."""
+    _check(lib().rv_greedy_head_noalloc(d_lm_head, d_final_norm, d_h, vocab, d_model, act_dtype, float(rms_eps),
+                                        d_next_id, d_logits, stream))
 
 
 def config_of(shape, max_batch: int, max_seq: int) -> RVConfig:

@@ -427,6 +427,10 @@ __global__ void k_set_scalars(int32_t *in, int Bmax, int mode, float tau, int en
 
 }  // namespace
 
+namespace rv {
+void set_error_message(const char *msg) { g_err = msg ? msg : ""; }
+}  // namespace rv
+
 // ==================================================================== C ABI
 
 extern "C" {

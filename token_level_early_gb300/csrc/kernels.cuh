@@ -126,4 +126,7 @@ cudaError_t launch_rtn_quantize(const uint16_t *W, int N, int K, int act, int g,
 cudaError_t launch_rope_table(float2 *cs, int T, int hd, double theta, cudaStream_t s);
 cudaError_t launch_fill_u16(uint16_t *p, size_t n, uint16_t v, cudaStream_t s);
 
+// Sets the calling thread's message returned by rv_last_error().
+void set_error_message(const char *msg);
+
 }  // namespace rv
