@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 
 import synth  # noqa: E402
 
+ENGINE_NAMES = {0: "chain", 1: "persistent"}
 METRIC = "decode tokens/s at bs1 (1B/8B shapes) and achieved HBM GB/s vs ~8 TB/s peak"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemv_gateup_llama8b.md")
 MODES = ("tau", "forced", "full", "river")
@@ -131,7 +132,7 @@ def token_bytes(shape, group, exit_layer, ctx):
 
 def kernel_hash():
     h = hashlib.sha256()
-    for f in ("decode_b1.cu", "kernels.cuh", "common.cuh"):
+    for f in ("decode_b1.cu", "gemv_core.cuh", "kernels.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "token_level_early_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -159,9 +160,11 @@ def profile_traffic():
 
 # ------------------------------------------------------------------ our arm
 
-def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=MODES):
+def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=MODES, engine_name="chain"):
     import torch
     import token_level_early_gb300 as rv
+
+    engine = {"chain": rv.ENGINE_CHAIN, "persistent": rv.ENGINE_PERSISTENT}[engine_name]
 
     wl = synth.WORKLOADS[wl_name]
     shape = wl.shape
@@ -172,17 +175,18 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
     w = synth.make_weights(shape)
     log(f"[{wl_name}] weights generated in {time.time() - t0:.1f}s")
     prompt = synth.make_prompt(shape.vocab, 1, wl.prompt_len)
-    max_seq = wl.prompt_len + len(MODES) * (warmup + steps) + steps + 72  # + room for the CPU baseline
+    max_seq = wl.prompt_len + (len(MODES) + 1) * (warmup + steps) + steps + 72  # + room for the CPU baseline
     stream = torch.cuda.Stream()
     t0 = time.time()
     m = rv.Model(shape, w, 1, max_seq, stream=stream.cuda_stream)
     m.quantize_river(wl.group, 1)
+    m.set_engine(engine)
     log(f"[{wl_name}] load + river in {time.time() - t0:.1f}s")
     t0 = time.time()
     first, e_seq = m.prefill(prompt, wl.prefill_tau)
     log(f"[{wl_name}] prefill {wl.prompt_len} tokens in {time.time() - t0:.1f}s, exit layer {int(e_seq[0])}")
 
-    n_ids = len(MODES) * (warmup + steps) + 1
+    n_ids = (len(MODES) + 1) * (warmup + steps) + 1
     d_ids = torch.zeros(n_ids, dtype=torch.int32, device="cuda")
     d_exit = torch.zeros_like(d_ids)
     d_forced = torch.from_numpy(np.concatenate([synth.forced_exits(i, 1, L) for i in range(warmup + steps)])).cuda()
@@ -224,6 +228,14 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
                          "bytes_per_token": by / steps}
         if clocks is not None:
             results[mode]["clocks"] = clocks
+
+    # the headline mode again on the other batch-1 engine, for comparison
+    other = rv.ENGINE_PERSISTENT if engine == rv.ENGINE_CHAIN else rv.ENGINE_CHAIN
+    m.set_engine(other)
+    run_mode(modes[0], warmup)
+    ms_c, _, _ = run_mode(modes[0], steps)
+    results[modes[0]][ENGINE_NAMES[other] + "_engine_tokens_per_s"] = steps / (ms_c / 1e3)
+    m.set_engine(engine)
 
     # e2e: the same tau-rule loop through the host-buffer API
     tok = int(d_ids[pos[0]].item())
@@ -313,6 +325,8 @@ def main():
     ap.add_argument("--workload", default="llama8b", choices=["llama8b", "llama1b", "layer8b"])
     ap.add_argument("--modes", default=",".join(MODES),
                     help="decode modes to time (tau, forced, full, river); the first is the headline")
+    ap.add_argument("--engine", default="chain", choices=["chain", "persistent"],
+                    help="batch-1 decode engine timed for the headline (the other is timed for comparison)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     args = ap.parse_args()
@@ -329,7 +343,7 @@ def main():
     cfg = {"workload": f"{wl.shape.name} decode, batch 1, {wl.prompt_len}-token random prompt, tau {tau}, "
                        f"river W4A16 group {wl.group}",
            "layers": wl.shape.n_layers, "d_model": wl.shape.d_model, "ffn": wl.shape.ffn, "vocab": wl.shape.vocab,
-           "batch": 1, "prompt_len": wl.prompt_len, "tau": tau, "river_group": wl.group,
+           "batch": 1, "prompt_len": wl.prompt_len, "tau": tau, "river_group": wl.group, "engine": args.engine,
            "parallelism": f"replicas{world}" if world > 1 else "single",
            "l2": "inputs larger than L2: every step streams GBs of weights (L2 is 129 MB)"}
 
@@ -358,7 +372,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     rv.lib()
     modes = tuple(x for x in args.modes.split(",") if x in MODES) or MODES
-    res = run_workload(args.workload, args.steps, args.warmup, local, not args.no_cpu_baseline, rank0, log, modes)
+    res = run_workload(args.workload, args.steps, args.warmup, local, not args.no_cpu_baseline, rank0, log, modes,
+                       args.engine)
     tau_r = res["modes"][modes[0]]
     ms = tau_r["ms_per_step"]
     e2e = res["e2e_tokens_per_s"]
@@ -371,7 +386,7 @@ def main():
     sec = None
     if not args.no_secondary and world == 1 and args.workload != "layer8b":
         other = "llama1b" if args.workload == "llama8b" else "llama8b"
-        r2 = run_workload(other, args.steps, args.warmup, local, False, rank0, log)
+        r2 = run_workload(other, args.steps, args.warmup, local, False, rank0, log, MODES, args.engine)
         t2 = r2["modes"]["tau"]
         sec = {"workload": other, "tokens_per_s": t2["tokens_per_s"], "achieved_gbs": t2["achieved_gbs"],
                "mean_exit_layer": t2["mean_exit_layer"],
@@ -400,7 +415,9 @@ def main():
             "roofline": roof, "kernels": res["kernels"], "cpu_baseline": res["cpu"],
             "e2e": {"value": world * e2e, "unit": "tokens/s", "h2d_bytes_per_step": 4 * 6,
                     "d2h_bytes_per_step": 4 * 4},
-            "gpu_launches": args.steps * (5 * L + 4), "clocks": tau_r.get("clocks"),
+            # per step: the scalar-setting kernel, then the captured chain (step init, embedding, five
+            # kernels per layer, LM head) or the one persistent kernel
+            "gpu_launches": args.steps * ((5 * L + 4) if args.engine == "chain" else 2), "clocks": tau_r.get("clocks"),
             "dtype_detail": "bf16 weights/activations/KV, int4 river weights with fp16 scale/zero, fp32 accumulation"}
     if sec:
         line["secondary"] = sec

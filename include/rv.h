@@ -153,6 +153,18 @@ int rv_set_debug(rv_model *m, int enable);
  * the buffer's size for max_batch rows (hidden, s, logits use B = max_batch). */
 int rv_debug_dump(rv_model *m, int what, void *dst, size_t bytes);
 
+/* Options (rv_set_option).  RV_OPT_DECODE_ENGINE selects how a batch-1
+ * decode step runs: RV_ENGINE_CHAIN (default) = a captured graph of one
+ * kernel per GEMV / attention, chained by programmatic dependent launch;
+ * RV_ENGINE_PERSISTENT = one cooperative launch of a persistent kernel with
+ * every block resident and grid barriers between the phases of a layer.
+ * Both compute the same step.  Returns RV_EINVAL for an unknown option or
+ * value, RV_ESTATE if the persistent kernel cannot be made resident. */
+#define RV_OPT_DECODE_ENGINE 0
+#define RV_ENGINE_CHAIN 0
+#define RV_ENGINE_PERSISTENT 1
+int rv_set_option(rv_model *m, int option, int value);
+
 /* Kernel timing for roofline reports: launch one batch-1 GEMV kernel of the
  * decode step `iters` times back to back on the model's stream (outside the
  * step graph) and return its mean device time per launch in *ms_per_launch

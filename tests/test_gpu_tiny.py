@@ -220,3 +220,38 @@ def test_device_pointer_variant(weights):
         gm2.sync_status()
     gm.close()
     gm2.close()
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama1b"])
+def test_decode_engines_agree(name):
+    """The persistent kernel and the per-kernel chain compute the same step
+    (attention split counts differ, so agreement is within tolerance)."""
+    wl = synth.WORKLOADS[name]
+    shape = wl.shape
+    w = synth.make_weights(shape) if name != "tiny" else synth.make_weights(TINY)
+    prompt = synth.make_prompt(shape.vocab, 1, 16, seed=8)
+    out = []
+    for engine in (rv.ENGINE_PERSISTENT, rv.ENGINE_CHAIN):
+        gm = rv.Model(shape, w, 1, 40)
+        gm.quantize_river(wl.group, 1)
+        gm.set_engine(engine)
+        gm.set_debug(True)
+        gm.prefill(prompt, 2.0, fixed_exit=shape.n_layers)
+        rec = []
+        tok = 7
+        for step in range(6):
+            f = np.array([(0, 2, shape.n_layers, 1, 3, 0)[step]], dtype=np.int32)
+            nxt, ex = gm.decode_step([tok], 0.9, f)
+            rec.append((int(nxt[0]), int(ex[0]), gm.dump(rv.DUMP_LOGITS)[0].copy(),
+                        gm.dump(rv.DUMP_HIDDEN)[:, 0].copy()))
+            tok = 5 + step
+        out.append(rec)
+        gm.close()
+    for (n1, e1, l1, h1), (n2, e2, l2, h2) in zip(*out):
+        assert e1 == e2
+        assert np.abs(l1 - l2).max() <= 5e-2
+        for l in range(h1.shape[0]):
+            assert rel_l2(h1[l], h2[l]) <= 1e-2
+        if n1 != n2:
+            srt = np.sort(l2)[::-1]
+            assert srt[0] - srt[1] < 1e-2

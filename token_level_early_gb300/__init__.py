@@ -20,7 +20,7 @@ _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "librv.so")
 _CSRC = os.path.join(_HERE, "csrc")
 _BUILD = os.path.join(_ROOT, "_build")
-SOURCES = ["api.cu", "decode_b1.cu", "attention.cu", "general.cu", "quant.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "decode_b1.cu", "attention.cu", "general.cu", "quant.cu", "noalloc.cu", "mega.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 RV_OK, RV_EINVAL, RV_ENOMEM, RV_ECUDA, RV_ECAPACITY, RV_ESTATE, RV_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
@@ -28,7 +28,9 @@ PROJ_Q, PROJ_K, PROJ_V, PROJ_O, PROJ_GATE, PROJ_UP, PROJ_DOWN = range(7)
 DUMP_HIDDEN, DUMP_S, DUMP_LOGITS, DUMP_KV, DUMP_LENS = range(5)
 EXPORTED = ("rv_last_error", "rv_load_model", "rv_quantize_river", "rv_export_river", "rv_prefill",
             "rv_decode_step", "rv_decode_step_dev", "rv_sync_status", "rv_kv_reset", "rv_set_debug",
-            "rv_debug_dump", "rv_kv_bytes", "rv_param_bytes", "rv_free_model", "rv_time_kernel", "rv_greedy_head_noalloc")
+            "rv_debug_dump", "rv_kv_bytes", "rv_param_bytes", "rv_free_model", "rv_time_kernel", "rv_greedy_head_noalloc",
+            "rv_set_option")
+OPT_DECODE_ENGINE, ENGINE_CHAIN, ENGINE_PERSISTENT = 0, 0, 1
 TIME_GATEUP, TIME_O, TIME_LMHEAD = 0, 1, 2
 
 
@@ -117,6 +119,7 @@ def lib():
         "rv_time_kernel": ([vp, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_float),
                             ctypes.POINTER(ctypes.c_double)], i32),
         "rv_greedy_head_noalloc": ([vp, vp, vp, i32, i32, i32, f32, vp, vp, vp], i32),
+        "rv_set_option": ([vp, i32, i32], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -226,6 +229,12 @@ class Model:
         else:
             r = np.ascontiguousarray(rows, dtype=np.int32)
             _check(lib().rv_kv_reset(self._h, _p(r), r.size))
+
+    def set_option(self, option: int, value: int):
+        _check(lib().rv_set_option(self._h, option, value))
+
+    def set_engine(self, engine: int):
+        self.set_option(OPT_DECODE_ENGINE, engine)
 
     def set_debug(self, enable: bool):
         _check(lib().rv_set_debug(self._h, 1 if enable else 0))

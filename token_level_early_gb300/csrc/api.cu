@@ -18,7 +18,9 @@
 
 #include "../../include/rv.h"
 #include "common.cuh"
+#include "gemv_core.cuh"
 #include "kernels.cuh"
+#include "mega.cuh"
 
 using namespace rv;
 
@@ -113,6 +115,14 @@ struct rv_model {
 
   // graphs
   std::map<int, cudaGraphExec_t> graphs;
+
+  // persistent batch-1 step
+  int engine = RV_ENGINE_CHAIN;
+  bool mega_ready = false;
+  int mega_grid = 0;
+  LayerDesc *d_layers = nullptr;
+  unsigned *bar = nullptr;
+  MegaArgs mega{};
 };
 
 namespace {
@@ -375,8 +385,69 @@ int enqueue_step_rows(rv_model *m, int B, cudaStream_t s) {
   return enqueue_head_rows(m, B, 1, -1, s);
 }
 
-// Capture (once per batch size) and launch the decode-step graph.
+// (Re)build the persistent kernel's argument block: layer descriptors (with
+// the river copies when built), activations, scratch, debug pointers.
+int build_mega(rv_model *m) {
+  m->mega_ready = false;
+  std::vector<LayerDesc> h(m->L);
+  size_t xs = 0;
+  for (int l = 0; l < m->L; ++l) {
+    for (int i = 0; i < N_MAT; ++i) {
+      h[l].m[i] = make_mat(m, m->layers[l], i);
+      const size_t f = x_floats(geo_of(h[l].m[i]));
+      if (f > xs) xs = f;
+    }
+    h[l].attn_norm = m->layers[l].attn_norm;
+    h[l].mlp_norm = m->layers[l].mlp_norm;
+  }
+  Mat lm{};
+  lm.w = m->lm_head; lm.N = m->V; lm.K = m->d;
+  if (x_floats(geo_of(lm)) > xs) xs = x_floats(geo_of(lm));
+  const size_t at = mega_attn_tile_floats(m->hd, m->H / m->Hkv);
+  if (at > xs) xs = at;
+  if ((size_t)mega_warps() * 32 * 2 > xs) xs = (size_t)mega_warps() * 32 * 2;  // head argmax scratch
+  RV_CK(cudaMemcpy(m->d_layers, h.data(), sizeof(LayerDesc) * m->L, cudaMemcpyHostToDevice));
+  MegaArgs &A = m->mega;
+  A = MegaArgs{};
+  A.layers = m->d_layers;
+  A.embed = m->embed; A.final_norm = m->final_norm; A.lm_head = m->lm_head;
+  A.L = m->L; A.d = m->d; A.H = m->H; A.Hkv = m->Hkv; A.hd = m->hd; A.F = m->F; A.V = m->V; A.act = m->act;
+  A.Bmax = m->Bmax;
+  A.eps = m->c.rms_eps;
+  A.kv = m->kv;
+  A.rope_cs = m->rope_cs;
+  A.st = m->st;
+  A.h[0] = m->hbuf[0]; A.h[1] = m->hbuf[1]; A.hmid = m->hmid; A.q = m->qbuf; A.o = m->obuf; A.a = m->abuf;
+  A.attn_part = m->attn_part;
+  int sp = m->n_sm / m->Hkv;
+  if (sp > m->attn_splits_max) sp = m->attn_splits_max;
+  A.splits = sp < 1 ? 1 : sp;
+  A.partials = m->partials;
+  A.bar = m->bar;
+  A.dbg_h = m->debug ? m->dbg_h : nullptr;
+  A.dbg_s = m->debug ? m->dbg_s : nullptr;
+  A.dbg_logits = m->debug ? m->dbg_logits : nullptr;
+  A.xs_floats = (xs + 3) & ~(size_t)3;
+  int grid = 0;
+  cudaError_t e = mega_prepare(A, m->n_sm, &grid);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return RV_OK;  // not resident on this device: the kernel chain serves
+  }
+  m->mega_grid = grid;
+  m->mega_ready = true;
+  return RV_OK;
+}
+
+// Launch one decode step (persistent kernel for batch 1 when selected, else
+// the captured graph for batch B, captured once per batch size).
 int launch_step(rv_model *m, int B) {
+  if (B == 1 && m->engine == RV_ENGINE_PERSISTENT && m->mega_ready) {
+    RV_CK(cudaMemsetAsync(m->st.err, 0, sizeof(int32_t), m->stream));
+    RV_CK(cudaMemsetAsync(m->bar, 0, sizeof(unsigned) * 2, m->stream));  // fresh barrier every step
+    RV_CK(mega_launch(m->mega, m->mega_grid, m->stream));
+    return RV_OK;
+  }
   auto it = m->graphs.find(B);
   if (it == m->graphs.end()) {
     if (B > 1) {
@@ -544,8 +615,11 @@ static int load_impl(rv_model *m, const rv_config *cfg, const void *const *weigh
   RV_ALLOC(A, m->gHf, sizeof(float) * (size_t)m->Bmax * d);
   RV_ALLOC(A, m->gXf, sizeof(float) * (size_t)m->Bmax * d);
   RV_ALLOC(A, m->gLogits, sizeof(float) * (size_t)m->Bmax * V);
+  RV_ALLOC(A, m->d_layers, sizeof(LayerDesc) * (size_t)m->L);
+  RV_ALLOC(A, m->bar, sizeof(unsigned) * 2);
+  RV_CK(cudaMemsetAsync(m->bar, 0, sizeof(unsigned) * 2, m->stream));
   RV_CK(cudaStreamSynchronize(m->stream));
-  return RV_OK;
+  return build_mega(m);
 }
 
 int rv_load_model(const rv_config *cfg, const void *const *weights, void *stream, rv_model **out) {
@@ -595,6 +669,7 @@ int rv_quantize_river(rv_model *m, int group_size, int entry_layer) {
   drop_graphs(m);
   free_list(m->river_allocs);
   m->has_river = false;
+  m->mega_ready = false;
   m->group = group_size;
   for (LayerDev &ly : m->layers)
     for (int i = 0; i < N_MAT; ++i) ly.r[i] = RiverDev{};
@@ -616,11 +691,12 @@ int rv_quantize_river(rv_model *m, int group_size, int entry_layer) {
   RV_CK(cudaStreamSynchronize(m->stream));
   if (err & 4) {
     free_list(m->river_allocs);
+    build_mega(m);
     return fail(RV_EINVAL, "a group's scale overflows fp16");
   }
   m->has_river = true;
   m->entry = entry_layer;
-  return RV_OK;
+  return build_mega(m);
 }
 
 int rv_export_river(const rv_model *m, int layer, int proj, void *q_packed, void *scales, void *zeros) {
@@ -819,6 +895,18 @@ int rv_set_debug(rv_model *m, int enable) {
   }
   if ((bool)enable != m->debug) drop_graphs(m);
   m->debug = enable != 0;
+  return build_mega(m);
+}
+
+int rv_set_option(rv_model *m, int option, int value) {
+  g_err.clear();
+  if (check_common(m)) return RV_EINVAL;
+  if (option != RV_OPT_DECODE_ENGINE) return fail(RV_EINVAL, "unknown option %d", option);
+  if (value != RV_ENGINE_CHAIN && value != RV_ENGINE_PERSISTENT) return fail(RV_EINVAL, "unknown engine %d", value);
+  if (value == RV_ENGINE_PERSISTENT && !m->mega_ready)
+    return fail(RV_ESTATE, "the persistent decode kernel cannot be made resident on this device");
+  RV_CK(cudaStreamSynchronize(m->stream));
+  m->engine = value;
   return RV_OK;
 }
 
