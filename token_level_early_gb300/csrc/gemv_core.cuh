@@ -10,13 +10,15 @@
 // transpose-reduce and, for S > 1, across the splits through shared memory;
 // the epilogue runs in the warp that owns the quad.
 //
-// int4 inner loop.  A code q becomes the float 1 + q/16 (nibble rotated into
-// mantissa bits 19..22 and the exponent of 1.0 OR-ed in) or 1 + q/256 (bits
-// 15..18): one funnel rotate per pair of codes and one LOP3 per code.  The
-// matching activation is pre-scaled by 16 or 256, so (1 + q/16)(16 x) =
-// 16 x + q x, and the constant sum of the pre-scaled activations is removed
-// once per 32 codes.  Products and sums are fp32 (packed fma.rn.f32x2), the
-// products exact.  Per 32 codes of a row: sum w x = s (sum q x - z sum x).
+// int4 inner loop.  One LOP3 turns two codes of a word into a pair of 16-bit
+// floats with the code in the low mantissa bits: bf16 128 + q (mask the
+// nibbles at bits 0..3 and 16..19, OR in the bits of 128.0), or fp16 1 + q/16
+// (nibbles shifted to bits 6..9 and 22..25, OR in 1.0).  Each code then takes
+// one mixed-precision FMA (16-bit operands, fp32 accumulator): the product of
+// the code value and a 16-bit activation is exact and only the fp32 sums
+// round.  Per lane run of 32 codes, with X the sum of its activations:
+//   bf16: sum (q - z) x = acc - (128 + z) X;   fp16: = 16 acc - (16 + z) X,
+// and the run adds s times that to the row.
 #pragma once
 
 #include "common.cuh"
@@ -53,39 +55,66 @@ __device__ __forceinline__ u64 ffma2(u64 a, u64 b, u64 c) {
   return d;
 }
 
-__device__ __forceinline__ uint32_t rotl(uint32_t x, int s) { return __funnelshift_l(x, x, s); }
+// d = (a & m) | c in one instruction (the compiler splits the two-constant
+// form into two).
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t m, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(m), "r"(c));
+  return d;
+}
 
-// One word of 8 codes (canonical nibble order) against its 4 activation
-// pairs.  Pair p holds (16 x[even nibble], 256 x[odd nibble]) for the nibble
-// pairs (0,7), (2,1), (4,3), (6,5).  Shifts bring each pair to mantissa bits
-// 19..22 (even) and 15..18 (odd): left shifts by 3 and 11 for (4,3) and
-// (2,1), a right shift by 5 for (6,5), and for (0,7) a left shift by 19 and a
-// right shift by 13.  Left shifts and the high half of a multiply (the right
-// shifts) run on the FMA pipe, leaving one LOP3 per code on the ALU pipe.
-__device__ __forceinline__ u64 word_fma(uint32_t w, const u64 *xp, u64 acc) {
-#ifdef RV_UNPACK_ROTATE
-  const int rot[4] = {19, 11, 3, 27};
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const uint32_t u = rotl(w, rot[p]);
-    const uint32_t fh = (u & 0x00780000u) | 0x3F800000u;  // 1 + q/16
-    const uint32_t fl = (u & 0x00078000u) | 0x3F800000u;  // 1 + q/256
-    acc = ffma2(((u64)fl << 32) | fh, xp[p], acc);
+// c + lo16(a) * lo16(b) and c + hi16(a) * hi16(b) with 16-bit operands of
+// type ACT (1 = bf16, 0 = fp16) and an fp32 accumulator.
+template <int ACT>
+__device__ __forceinline__ float fma_lo16(uint32_t a, uint32_t b, float c) {
+  float d;
+  if (ACT == 1)
+    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.bf16 %0, al, bl, %3;}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  else
+    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.f16 %0, al, bl, %3;}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+template <int ACT>
+__device__ __forceinline__ float fma_hi16(uint32_t a, uint32_t b, float c) {
+  float d;
+  if (ACT == 1)
+    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.bf16 %0, ah, bh, %3;}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  else
+    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.f16 %0, ah, bh, %3;}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
+// Code extraction constants (mask, OR-ed bits) by activation type.
+template <int ACT>
+struct CodeBits {
+  static constexpr uint32_t mask = ACT == 1 ? 0x000F000Fu : 0x03C003C0u;
+  static constexpr uint32_t one = ACT == 1 ? 0x43004300u : 0x3C003C00u;
+  static constexpr float A = ACT == 1 ? 1.f : 16.f;    // sum (q - z) x = A acc - (B + z) X
+  static constexpr float B = ACT == 1 ? 128.f : 16.f;
+};
+
+// One word of 8 codes (canonical nibble order: code i at bits 4i..4i+3)
+// against its activation pairs xr[p] = (x[p], x[p + 4]) as 16-bit pairs.
+// a0 collects codes 0..3, a1 codes 4..7.
+template <int ACT>
+__device__ __forceinline__ void word_mix(uint32_t w, const uint32_t *xr, float &a0, float &a1, uint32_t m,
+                                         uint32_t one) {
+  uint32_t u0, u1, u2, u3;
+  if (ACT == 1) {
+    u0 = w; u1 = w >> 4; u2 = w >> 8; u3 = w >> 12;
+  } else {
+    u0 = w << 6; u1 = w << 2; u2 = w >> 2; u3 = w >> 6;
   }
-#else
-  const uint32_t u0h = w << 19, u0l = __umulhi(w, 1u << 19);  // nibble 0 -> 19..22, 7 -> 15..18
-  const uint32_t u1 = w << 11;                                // nibbles 2, 1
-  const uint32_t u2 = w << 3;                                 // nibbles 4, 3
-  const uint32_t u3 = __umulhi(w, 1u << 27);                  // nibbles 6, 5
-  const uint32_t hs[4] = {u0h, u1, u2, u3}, ls[4] = {u0l, u1, u2, u3};
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const uint32_t fh = (hs[p] & 0x00780000u) | 0x3F800000u;  // 1 + q/16
-    const uint32_t fl = (ls[p] & 0x00078000u) | 0x3F800000u;  // 1 + q/256
-    acc = ffma2(((u64)fl << 32) | fh, xp[p], acc);
-  }
-#endif
-  return acc;
+  const uint32_t c0 = lop3_and_or(u0, m, one), c1 = lop3_and_or(u1, m, one);
+  const uint32_t c2 = lop3_and_or(u2, m, one), c3 = lop3_and_or(u3, m, one);
+  a0 = fma_lo16<ACT>(c0, xr[0], a0); a1 = fma_hi16<ACT>(c0, xr[0], a1);
+  a0 = fma_lo16<ACT>(c1, xr[1], a0); a1 = fma_hi16<ACT>(c1, xr[1], a1);
+  a0 = fma_lo16<ACT>(c2, xr[2], a0); a1 = fma_hi16<ACT>(c2, xr[2], a1);
+  a0 = fma_lo16<ACT>(c3, xr[3], a0); a1 = fma_hi16<ACT>(c3, xr[3], a1);
 }
 
 // Two 16-bit weights of a word times their activations (packed fp32 FMA).
@@ -149,6 +178,7 @@ __device__ __forceinline__ bool last_block(unsigned *counter) {
 
 struct Geo {
   int K, Kp, nk4, nk16, words, G;
+  int gpc;  // groups per int4 chunk when the group size divides the chunk, else 0
 };
 
 __host__ __device__ __forceinline__ Geo geo_of(const Mat &m) {
@@ -159,6 +189,7 @@ __host__ __device__ __forceinline__ Geo geo_of(const Mat &m) {
   g.nk16 = (m.K + CH16 - 1) / CH16;
   g.words = g.Kp >> 3;
   g.G = m.r.G;
+  g.gpc = (m.r.g > 0 && CH4 % m.r.g == 0) ? CH4 / m.r.g : 0;
   return g;
 }
 
@@ -173,7 +204,7 @@ constexpr int STAGE = STAGE_W + STAGE_S;
 // Shared memory (bytes): activations in the lane layout of the larger path,
 // 256 floats of reduction scratch, then the warps' staging rings.
 __host__ __device__ __forceinline__ size_t x_floats(const Geo &g) {
-  const size_t river = (size_t)g.nk4 * (8 * 32 * 4 + 32 * 2);
+  const size_t river = (size_t)g.nk4 * (4 * 32 * 4 + 32);
   const size_t b16 = (size_t)g.nk16 * (2 * 32 * 4);
   return river > b16 ? river : b16;
 }
@@ -219,43 +250,77 @@ __host__ __device__ __forceinline__ int splits_for(int nquads, int nk) {
 }
 
 // The warp's stream of work items (quad, chunk) in consumption order: quads
-// bq + rg for bq = bid * RG, + nblocks * RG, ...; chunks sp, sp + S, ...
+// bq + rg for bq = bid * RG, + nblocks * RG, ...; chunks sp, sp + S, ...  Every
+// quad is two row pairs (rows[0], rows[0] + 1) and (rows[2], rows[2] + 1); the
+// offsets of rows[0] and rows[2] in the quad being issued (int4 words or
+// 16-bit elements, and (scale, zero) words) are cached and recomputed when the
+// quad changes.
 struct ItemStream {
   int bq, c, step;
+  uint32_t off0, off2, soff0, soff2;
 };
 
 template <int EPI>
+__device__ __forceinline__ void stream_rows(const GemvArgs &a, const Geo &g, int river, int qd, ItemStream &is) {
+  int rows[4];
+  quad_rows<EPI>(a, qd, rows);
+  const uint32_t stride = (uint32_t)(river ? g.words : g.K);
+  is.off0 = (uint32_t)rows[0] * stride;
+  is.off2 = (uint32_t)rows[2] * stride;
+  is.soff0 = (uint32_t)rows[0] * (uint32_t)g.G;
+  is.soff2 = (uint32_t)rows[2] * (uint32_t)g.G;
+}
+
+__device__ __forceinline__ void cp16s(unsigned dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp4s(unsigned dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Copy the next item of the stream into `stage` (one commit group per call,
+// empty once the stream has ended).  lane_g: the lane's group within a chunk.
+template <int EPI>
 __device__ __forceinline__ void issue_item(const GemvArgs &a, const Geo &g, int river, int rg, int nquads, int nk,
-                                           int S, int sp, int RG, ItemStream &is, char *stage, int lane) {
+                                           int S, int sp, int lane_g, ItemStream &is, char *stage, int lane) {
   if (is.bq + rg < nquads) {
-    int rows[4];
-    quad_rows<EPI>(a, is.bq + rg, rows);
+    const unsigned sd = (unsigned)__cvta_generic_to_shared(stage) + lane * 16;
     if (river) {
       const int k0 = is.c * CH4 + lane * 32;
       if (k0 < g.Kp) {
-        const RiverMat &R = a.m.r;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          cp16(stage + (r * 32 + lane) * 16, R.q + (size_t)rows[r] * g.words + (k0 >> 3));
-          cp4(stage + STAGE_W + (r * 32 + lane) * 4, R.sz + (size_t)rows[r] * g.G + k0 / R.g);
-        }
+        const uint32_t *qb = a.m.r.q + (k0 >> 3);
+        const __half2 *sb = a.m.r.sz + (g.gpc ? is.c * g.gpc + lane_g : k0 / a.m.r.g);
+        const unsigned ss = (unsigned)__cvta_generic_to_shared(stage) + STAGE_W + lane * 4;
+        const uint32_t *q0 = qb + is.off0, *q2 = qb + is.off2;
+        const __half2 *s0 = sb + is.soff0, *s2 = sb + is.soff2;
+        cp16s(sd, q0);
+        cp16s(sd + 512, q0 + g.words);
+        cp16s(sd + 1024, q2);
+        cp16s(sd + 1536, q2 + g.words);
+        cp4s(ss, s0);
+        cp4s(ss + 128, s0 + g.G);
+        cp4s(ss + 256, s2);
+        cp4s(ss + 384, s2 + g.G);
       }
     } else {
       const int k0 = is.c * CH16 + lane * 8;
       if (k0 < g.K) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) cp16(stage + (r * 32 + lane) * 16, a.m.w + (size_t)rows[r] * g.K + k0);
+        const uint16_t *w0 = a.m.w + k0 + is.off0, *w2 = a.m.w + k0 + is.off2;
+        cp16s(sd, w0);
+        cp16s(sd + 512, w0 + g.K);
+        cp16s(sd + 1024, w2);
+        cp16s(sd + 1536, w2 + g.K);
       }
     }
     is.c += S;
     if (is.c >= nk) {
       is.c = sp;
       is.bq += is.step;
+      if (is.bq + rg < nquads) stream_rows<EPI>(a, g, river, is.bq + rg, is);
     }
   }
-  cp_commit();  // one group per item slot, empty once the stream has ended
+  cp_commit();
 }
-
 
 // Per-thread results of a GEMV phase that the caller combines across blocks:
 // the s(l) sums of the down projection, the argmax candidate of the LM head.
@@ -266,7 +331,7 @@ struct PhaseOut {
 
 struct PhaseGeo {
   Geo g;
-  int river, nk, S, RG, rg, sp, nquads;
+  int river, nk, S, RG, rg, sp, nquads, lane_g;
 };
 
 template <int NWARP>
@@ -281,6 +346,7 @@ __device__ __forceinline__ PhaseGeo phase_geo(const GemvArgs &a, int river) {
   p.rg = warp / p.S;
   p.sp = warp % p.S;
   p.nquads = a.m.N >> 2;
+  p.lane_g = (river && p.g.gpc) ? ((threadIdx.x & 31) * 32) / a.m.r.g : 0;
   return p;
 }
 
@@ -291,10 +357,14 @@ template <int NWARP, int EPI>
 __device__ __forceinline__ ItemStream gemv_begin(const GemvArgs &a, int river, char *ring, int bid, int nblocks) {
   const PhaseGeo p = phase_geo<NWARP>(a, river);
   const int lane = threadIdx.x & 31;
-  ItemStream is{bid * p.RG, p.sp, nblocks * p.RG};
+  ItemStream is;
+  is.bq = bid * p.RG;
+  is.c = p.sp;
+  is.step = nblocks * p.RG;
+  if (is.bq + p.rg < p.nquads) stream_rows<EPI>(a, p.g, river, is.bq + p.rg, is);
 #pragma unroll
   for (int i = 0; i < NST - 1; ++i)
-    issue_item<EPI>(a, p.g, river, p.rg, p.nquads, p.nk, p.S, p.sp, p.RG, is, ring + i * STAGE, lane);
+    issue_item<EPI>(a, p.g, river, p.rg, p.nquads, p.nk, p.S, p.sp, p.lane_g, is, ring + i * STAGE, lane);
   return is;
 }
 
@@ -323,24 +393,23 @@ __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float
     rs = 1.0f / sqrtf(ss / (float)g.K + a.eps);
   }
   if (river) {
-    float4 *xq = reinterpret_cast<float4 *>(xs);                    // [nk][8][32]
-    float2 *cx = reinterpret_cast<float2 *>(xs + nk * 8 * 32 * 4);  // [nk][32] (C, X)
+    uint4 *xq = reinterpret_cast<uint4 *>(xs);       // [nk][4][32]: word j's pairs (x[8j+p], x[8j+p+4])
+    float *xsum = xs + nk * 4 * 32 * 4;              // [nk][32]: sum of the lane run's 32 activations
     for (int t = tid; t < nk * 32; t += blockDim.x) {
       const int c = t >> 5, ln = t & 31, base = c * CH4 + ln * 32;
-      float C = 0.f, X = 0.f;
+      float X = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int j = 0; j < 4; ++j) {
         float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (base + 8 * i < g.K) load_x8<ACT, PRO>(a, base + 8 * i, rs, x);
-        // pairs (even, odd) = (0,7), (2,1), (4,3), (6,5), scaled by 16 and 256
-        const float e0 = 16.f * x[0], o0 = 256.f * x[7], e1 = 16.f * x[2], o1 = 256.f * x[1];
-        const float e2 = 16.f * x[4], o2 = 256.f * x[3], e3 = 16.f * x[6], o3 = 256.f * x[5];
-        xq[(c * 8 + 2 * i) * 32 + ln] = make_float4(e0, o0, e1, o1);
-        xq[(c * 8 + 2 * i + 1) * 32 + ln] = make_float4(e2, o2, e3, o3);
-        C += ((e0 + o0) + (e1 + o1)) + ((e2 + o2) + (e3 + o3));
+        if (base + 8 * j < g.K) load_x8<ACT, PRO>(a, base + 8 * j, rs, x);
+        uint32_t pr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          pr[i] = (uint32_t)f_to_act(x[i], ACT) | ((uint32_t)f_to_act(x[i + 4], ACT) << 16);
+        xq[(c * 4 + j) * 32 + ln] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
         X += ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
       }
-      cx[c * 32 + ln] = make_float2(C, X);
+      xsum[c * 32 + ln] = X;
     }
   } else {
     float4 *xb = reinterpret_cast<float4 *>(xs);  // [nk][2][32]
@@ -356,6 +425,10 @@ __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float
 
   const int pos = (EPI == EPI_QKV) ? a.st.len[0] : 0;
   PhaseOut out{0.f, 0.f, 0.f, -INFINITY, 0x7fffffff};
+  // code extraction constants in registers (a two-immediate LOP3 is split in two)
+  uint32_t cm, c1;
+  asm("mov.b32 %0, %1;" : "=r"(cm) : "n"(CodeBits<ACT>::mask));
+  asm("mov.b32 %0, %1;" : "=r"(c1) : "n"(CodeBits<ACT>::one));
   int parity = 0, t = 0;
 
   for (int base_q = bid * RG; base_q < nquads; base_q += nblocks * RG, parity ^= 1) {
@@ -367,31 +440,33 @@ __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float
       u64 acc[4] = {0ull, 0ull, 0ull, 0ull};
       for (int c = sp; c < nk; c += S, ++t) {
         cp_wait<NST - 2>();  // this lane's copies of item t have landed
-        issue_item<EPI>(a, g, river, rg, nquads, nk, S, sp, RG, is, ring + ((t + NST - 1) % NST) * STAGE, lane);
-        const char *stg = ring + (t % NST) * STAGE;
+        issue_item<EPI>(a, g, river, rg, nquads, nk, S, sp, p.lane_g, is, ring + ((t + NST - 1) & (NST - 1)) * STAGE,
+                        lane);
+        const char *stg = ring + (t & (NST - 1)) * STAGE;
         const uint4 *sw = reinterpret_cast<const uint4 *>(stg);
         if (river) {
           const int k0 = c * CH4 + lane * 32;
           if (k0 >= g.Kp) continue;
-          const float4 *xq = reinterpret_cast<const float4 *>(xs);
-          const float2 cxv = reinterpret_cast<const float2 *>(xs + nk * 8 * 32 * 4)[c * 32 + lane];
+          const uint4 *xq = reinterpret_cast<const uint4 *>(xs) + c * 4 * 32 + lane;
+          const float X = xs[nk * 4 * 32 * 4 + c * 32 + lane];
           const __half2 *ss = reinterpret_cast<const __half2 *>(stg + STAGE_W);
-          u64 xp[16];
+          uint32_t xr[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 f = xq[(c * 8 + i) * 32 + lane];
-            xp[2 * i] = pack2(f.x, f.y);
-            xp[2 * i + 1] = pack2(f.z, f.w);
+          for (int j = 0; j < 4; ++j) {
+            const uint4 f = xq[j * 32];
+            xr[4 * j] = f.x; xr[4 * j + 1] = f.y; xr[4 * j + 2] = f.z; xr[4 * j + 3] = f.w;
           }
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const uint4 w = sw[r * 32 + lane];
-            u64 ac = word_fma(w.x, xp + 0, 0ull);
-            ac = word_fma(w.y, xp + 4, ac);
-            u64 ad = word_fma(w.z, xp + 8, 0ull);
-            ad = word_fma(w.w, xp + 12, ad);
+            float a0 = 0.f, a1 = 0.f;
+            word_mix<ACT>(w.x, xr + 0, a0, a1, cm, c1);
+            word_mix<ACT>(w.y, xr + 4, a0, a1, cm, c1);
+            word_mix<ACT>(w.z, xr + 8, a0, a1, cm, c1);
+            word_mix<ACT>(w.w, xr + 12, a0, a1, cm, c1);
             const float2 sz = __half22float2(ss[r * 32 + lane]);
-            v[r] = fmaf(sz.x, (sum2(ac) + sum2(ad)) - fmaf(sz.y, cxv.y, cxv.x), v[r]);
+            const float run = fmaf(CodeBits<ACT>::A, a0 + a1, -(CodeBits<ACT>::B + sz.y) * X);
+            v[r] = fmaf(sz.x, run, v[r]);
           }
         } else {
           const int k0 = c * CH16 + lane * 8;
