@@ -98,7 +98,7 @@ struct rv_model {
   float *hbuf[2] = {nullptr, nullptr}, *hmid = nullptr, *qbuf = nullptr, *obuf = nullptr, *abuf = nullptr;
   float *partials = nullptr;
   unsigned *counters = nullptr;
-  int attn_splits_b1 = 1, attn_splits_max = 1;
+  int attn_splits_b1 = 1, attn_splits_max = 1, attn_cluster = 1;
   float *attn_part = nullptr;
   unsigned *attn_counter = nullptr;
 
@@ -328,10 +328,9 @@ int enqueue_layer_rows(rv_model *m, int l, int B, int T, const int32_t *base, cu
     at.kv = m->kv; at.layer = l; at.H = m->H; at.Hkv = m->Hkv; at.hd = m->hd; at.act = act;
     at.q = m->gQ; at.o = m->gO; at.len = base; at.splits = m->attn_splits_max;
     at.part = m->attn_part; at.counter = m->attn_counter;
-    // decode rows: split count sized for the batch
-    int sp = (2 * m->n_sm + m->Hkv * B - 1) / (m->Hkv * B);
-    if (sp < 1) sp = 1;
-    if (sp > m->attn_splits_max) sp = m->attn_splits_max;
+    // decode rows: cluster size (a power of two) sized for the batch
+    int sp = 1;
+    while (2 * sp <= m->attn_cluster && 2 * sp * m->Hkv * B <= 2 * m->n_sm) sp *= 2;
     at.splits = sp;
     RV_CK(launch_attn_decode(at, B, s));
   } else {
@@ -606,8 +605,11 @@ static int load_impl(rv_model *m, const rv_config *cfg, const void *const *weigh
   if (sp > tiles) sp = tiles;
   if (sp > 128) sp = 128;
   if (sp < 1) sp = 1;
-  m->attn_splits_b1 = sp;
-  m->attn_splits_max = sp;
+  m->attn_splits_max = sp;  // split count of the persistent kernel's attention
+  // decode attention: one cluster of splits per (row, kv head)
+  m->attn_cluster = attn_dec_max_cluster(m->hd, m->H / m->Hkv, m->act);
+  if (m->attn_cluster < 1) return fail(RV_ECUDA, "decode attention cannot be launched on this device");
+  m->attn_splits_b1 = m->attn_cluster;
   RV_ALLOC(A, m->attn_part, sizeof(float) * (size_t)m->Bmax * m->H * sp * (m->hd + 2));
   RV_ALLOC(A, m->attn_counter, sizeof(unsigned) * (size_t)m->Bmax * m->Hkv);
   RV_CK(cudaMemsetAsync(m->attn_counter, 0, sizeof(unsigned) * (size_t)m->Bmax * m->Hkv, m->stream));

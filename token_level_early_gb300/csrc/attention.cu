@@ -9,10 +9,20 @@
 // merges the partial softmax states.  The single KV cache is the one every
 // backbone and river layer writes (paperlayer.ai section 4 / appendix A.3;
 // aitrends.kr KV Share).
+//
+// Decode rows use k_attn_dec: the splits of one (row, kv head) form a
+// thread-block cluster.  Each split streams its share of the past positions
+// 0..p-1 (final before the step starts) through a shared-memory ring that it
+// fills before the programmatic-dependent-launch wait; only q and the K/V of
+// position p come from the QKV kernel it follows.  The splits merge their
+// softmax states through distributed shared memory.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "common.cuh"
 #include "kernels.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace rv {
 
@@ -128,6 +138,234 @@ __global__ void __launch_bounds__(GRP * 32) k_attn(AttnArgs a, int T_per_row, co
   for (int r = 0; r < PER; ++r) a.o[orow + lane + 32 * r] = round_act(acc[r] * inv, a.act);
 }
 
+// ---- decode: clustered split-KV attention ----------------------------------
+constexpr int DTT = 32;   // positions per tile (one per lane in the score pass)
+constexpr int DNST = 4;   // ring stages
+
+template <int HD>
+struct DecTile {
+  static constexpr int KROW = HD * 2 + 16;  // padded K row: lane-per-row 16-byte reads hit distinct banks
+  static constexpr int VROW = HD * 2;
+  static constexpr int BYTES = DTT * (KROW + VROW);
+};
+
+template <int HD>
+static size_t dec_smem(int grp) {
+  return (size_t)DNST * DecTile<HD>::BYTES + sizeof(float) * grp * (HD + 2);
+}
+
+__device__ __forceinline__ uint32_t pack_act2(float lo, float hi, int act) {
+  return (uint32_t)f_to_act(lo, act) | ((uint32_t)f_to_act(hi, act) << 16);
+}
+
+template <int HD, int GRP, int ACT>
+__global__ void __launch_bounds__(GRP * 32, 1) k_attn_dec(AttnArgs a) {
+  using TL = DecTile<HD>;
+  constexpr int NT = GRP * 32, PER = HD / 32, PR = HD / 8;
+  extern __shared__ __align__(16) unsigned char sm[];
+  float *part = reinterpret_cast<float *>(sm + DNST * TL::BYTES);  // [GRP][HD + 2]: o, running max, sum
+  cg::cluster_group cl = cg::this_cluster();
+  const int cs = (int)cl.num_blocks(), sp = (int)cl.block_rank();
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // The token sits at position p = len[b] (advanced by the previous step's
+  // LM-head kernel, final here); positions < p were written by earlier steps.
+  const int p = a.len[b];
+  const int ntile = (p + DTT - 1) / DTT;
+  const int per = (ntile + cs - 1) / cs;
+  const int tb = min(ntile, sp * per), te = min(ntile, tb + per);
+  const uint16_t *Kb = a.kv.base + a.kv.idx(a.layer, 0, b, g, 0);
+  const uint16_t *Vb = a.kv.base + a.kv.idx(a.layer, 1, b, g, 0);
+  const unsigned sbase = (unsigned)__cvta_generic_to_shared(sm);
+
+  auto issue = [&](int tile, int slot) {
+    if (tile < te) {
+      const int t0 = tile * DTT, n = min(DTT, p - t0);
+      const unsigned st = sbase + slot * TL::BYTES;
+      for (int v = tid; v < 2 * DTT * PR; v += NT) {
+        const int kv = v >= DTT * PR, rem = v - kv * DTT * PR, t = rem / PR, c = rem - t * PR;
+        if (t < n) {
+          const uint16_t *src = (kv ? Vb : Kb) + (size_t)(t0 + t) * HD + c * 8;
+          cp16s(st + (kv ? DTT * TL::KROW + t * TL::VROW : t * TL::KROW) + c * 16, src);
+        }
+      }
+    }
+    cp_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < DNST - 1; ++i) issue(tb + i, i);
+
+  pdl_wait();
+  pdl_trigger();
+
+  // q of head h as 16-bit pairs (q is act-rounded after RoPE: exact)
+  const int h = g * GRP + warp;
+  const float *qp = a.q + ((size_t)b * a.H + h) * HD;
+  uint32_t qr[HD / 2];
+#pragma unroll
+  for (int i = 0; i < HD / 4; ++i) {
+    const float4 v = *reinterpret_cast<const float4 *>(qp + 4 * i);
+    qr[2 * i] = pack_act2(v.x, v.y, ACT);
+    qr[2 * i + 1] = pack_act2(v.z, v.w, ACT);
+  }
+  const float scale = 1.0f / sqrtf((float)HD);
+  float mrun = -INFINITY, lrun = 0.f, o[PER];
+#pragma unroll
+  for (int r = 0; r < PER; ++r) o[r] = 0.f;
+
+  for (int tile = tb, it = 0; tile < te; ++tile, ++it) {
+    cp_wait<DNST - 2>();
+    __syncthreads();  // the tile is in; every warp is done with the slot refilled next
+    issue(tile + DNST - 1, (it + DNST - 1) % DNST);
+    const unsigned char *tk = sm + (it % DNST) * TL::BYTES;
+    const unsigned char *tv = tk + DTT * TL::KROW;
+    const int n = min(DTT, p - tile * DTT);
+    float sc = -INFINITY;
+    if (lane < n) {
+      const uint4 *kr = reinterpret_cast<const uint4 *>(tk + lane * TL::KROW);
+      float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+      for (int j = 0; j < PR; ++j) {
+        const uint4 k = kr[j];
+        d0 = fma_lo16<ACT>(k.x, qr[4 * j], d0);
+        d1 = fma_hi16<ACT>(k.x, qr[4 * j], d1);
+        d2 = fma_lo16<ACT>(k.y, qr[4 * j + 1], d2);
+        d3 = fma_hi16<ACT>(k.y, qr[4 * j + 1], d3);
+        d0 = fma_lo16<ACT>(k.z, qr[4 * j + 2], d0);
+        d1 = fma_hi16<ACT>(k.z, qr[4 * j + 2], d1);
+        d2 = fma_lo16<ACT>(k.w, qr[4 * j + 3], d2);
+        d3 = fma_hi16<ACT>(k.w, qr[4 * j + 3], d3);
+      }
+      sc = ((d0 + d1) + (d2 + d3)) * scale;
+    }
+    const float mnew = fmaxf(mrun, warp_max(sc));
+    const float pe = lane < n ? expf(sc - mnew) : 0.f;
+    const float corr = mrun == -INFINITY ? 0.f : expf(mrun - mnew);
+    lrun = lrun * corr + warp_sum(pe);
+#pragma unroll
+    for (int r = 0; r < PER; ++r) o[r] *= corr;
+    for (int t = 0; t < n; ++t) {
+      const float pt = __shfl_sync(0xffffffffu, pe, t);
+      const uint16_t *vr = reinterpret_cast<const uint16_t *>(tv + t * TL::VROW) + lane * PER;
+      if constexpr (PER == 4) {
+        const uint2 vv = *reinterpret_cast<const uint2 *>(vr);
+        o[0] = fmaf(pt, act_to_f((uint16_t)(vv.x & 0xFFFFu), ACT), o[0]);
+        o[1] = fmaf(pt, act_to_f((uint16_t)(vv.x >> 16), ACT), o[1]);
+        o[2] = fmaf(pt, act_to_f((uint16_t)(vv.y & 0xFFFFu), ACT), o[2]);
+        o[3] = fmaf(pt, act_to_f((uint16_t)(vv.y >> 16), ACT), o[3]);
+      } else {
+        const uint32_t vv = *reinterpret_cast<const uint32_t *>(vr);
+        o[0] = fmaf(pt, act_to_f((uint16_t)(vv & 0xFFFFu), ACT), o[0]);
+        o[1] = fmaf(pt, act_to_f((uint16_t)(vv >> 16), ACT), o[1]);
+      }
+    }
+    mrun = mnew;
+  }
+
+  // position p itself (its K/V were written by the QKV kernel this kernel
+  // follows): folded in by the last split
+  if (sp == cs - 1) {
+    const uint16_t *kc = Kb + (size_t)p * HD + lane * PER, *vc = Vb + (size_t)p * HD + lane * PER;
+    float d = 0.f;
+#pragma unroll
+    for (int r = 0; r < PER; ++r) d = fmaf(qp[lane * PER + r], act_to_f(kc[r], ACT), d);
+    const float sc = warp_sum(d) * scale;
+    const float mnew = fmaxf(mrun, sc);
+    const float corr = mrun == -INFINITY ? 0.f : expf(mrun - mnew), pe = expf(sc - mnew);
+    lrun = lrun * corr + pe;
+#pragma unroll
+    for (int r = 0; r < PER; ++r) o[r] = fmaf(pe, act_to_f(vc[r], ACT), o[r] * corr);
+    mrun = mnew;
+  }
+
+  // merge across the cluster: split sp combines dims [sp * HD / cs, ...) of every head
+  float *pp = part + warp * (HD + 2);
+#pragma unroll
+  for (int r = 0; r < PER; ++r) pp[lane * PER + r] = o[r];
+  if (lane == 0) {
+    pp[HD] = mrun;
+    pp[HD + 1] = lrun;
+  }
+  cl.sync();
+  const int dpc = HD / cs;
+  for (int e = tid; e < GRP * dpc; e += NT) {
+    const int hh = e / dpc, dd = sp * dpc + (e - hh * dpc);
+    float M = -INFINITY;
+    for (int r = 0; r < cs; ++r) M = fmaxf(M, cl.map_shared_rank(part, r)[hh * (HD + 2) + HD]);
+    float Ls = 0.f, O = 0.f;
+    for (int r = 0; r < cs; ++r) {
+      const float *rp = cl.map_shared_rank(part, r) + hh * (HD + 2);
+      const float w = rp[HD] == -INFINITY ? 0.f : expf(rp[HD] - M);
+      Ls = fmaf(w, rp[HD + 1], Ls);
+      O = fmaf(w, rp[dd], O);
+    }
+    a.o[((size_t)b * a.H + g * GRP + hh) * HD + dd] = round_act(O * (1.0f / Ls), ACT);
+  }
+  cl.sync();  // every split's partials stay readable until all merges are done
+}
+
+template <int HD, int GRP, int ACT>
+static cudaError_t launch_dec(const AttnArgs &a, int B, int cs, cudaStream_t s, int pdl) {
+  auto fn = k_attn_dec<HD, GRP, ACT>;
+  const size_t smem = dec_smem<HD>(GRP);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess && cs > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, a.Hkv, B);
+  cfg.blockDim = dim3(GRP * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  e = cudaLaunchKernelEx(&cfg, fn, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Largest cluster size (power of two, <= 16) the decode attention can be
+// launched with on this device; 0 if none.
+int attn_dec_max_cluster(int hd, int grp, int act) {
+  for (int cs = 16; cs >= 1; cs >>= 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, 1, 1);
+    cfg.blockDim = dim3(grp * 32);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = cudaErrorInvalidValue;
+#define RV_DQ(HD_, G_, A_)                                                                                   \
+  if (hd == HD_ && grp == G_ && act == A_) {                                                                 \
+    auto fn = k_attn_dec<HD_, G_, A_>;                                                                       \
+    cfg.dynamicSmemBytes = dec_smem<HD_>(G_);                                                                \
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);    \
+    if (e == cudaSuccess && cs > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1); \
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);                                  \
+  }
+    RV_DQ(64, 1, 0) RV_DQ(64, 2, 0) RV_DQ(64, 4, 0) RV_DQ(64, 8, 0)
+    RV_DQ(128, 1, 0) RV_DQ(128, 2, 0) RV_DQ(128, 4, 0) RV_DQ(128, 8, 0)
+    RV_DQ(64, 1, 1) RV_DQ(64, 2, 1) RV_DQ(64, 4, 1) RV_DQ(64, 8, 1)
+    RV_DQ(128, 1, 1) RV_DQ(128, 2, 1) RV_DQ(128, 4, 1) RV_DQ(128, 8, 1)
+#undef RV_DQ
+    if (e == cudaSuccess && n > 0) return cs;
+    cudaGetLastError();
+  }
+  return 0;
+}
+
 template <int HD, int GRP>
 static cudaError_t launch_hg(const AttnArgs &a, int T_per_row, const int32_t *base, int rows, cudaStream_t s,
                              int pdl) {
@@ -146,9 +384,18 @@ static cudaError_t launch_any(const AttnArgs &a, int T_per_row, const int32_t *b
   return cudaErrorInvalidValue;
 }
 
-// Decode: one row per batch entry, the token at position len[b].
+// Decode: one row per batch entry, the token at position len[b]; a.splits is
+// the cluster size (a power of two <= 16 that attn_dec_max_cluster allows).
 cudaError_t launch_attn_decode(const AttnArgs &a, int B, cudaStream_t s, int pdl) {
-  return launch_any(a, 1, a.len, B, s, pdl);
+  const int grp = a.H / a.Hkv, cs = a.splits;
+  if (cs < 1 || cs > 16 || (cs & (cs - 1))) return cudaErrorInvalidValue;
+#define RV_DL(HD_, G_)                                                                  \
+  if (a.hd == HD_ && grp == G_)                                                         \
+    return a.act == 1 ? launch_dec<HD_, G_, 1>(a, B, cs, s, pdl) : launch_dec<HD_, G_, 0>(a, B, cs, s, pdl);
+  RV_DL(64, 1) RV_DL(64, 2) RV_DL(64, 4) RV_DL(64, 8)
+  RV_DL(128, 1) RV_DL(128, 2) RV_DL(128, 4) RV_DL(128, 8)
+#undef RV_DL
+  return cudaErrorInvalidValue;
 }
 
 // Prefill / general rows: T tokens per sequence starting at base (NULL = 0).

@@ -121,4 +121,49 @@ struct KVGeom {
   }
 };
 
+// cp.async: 16- and 4-byte global -> shared copies, commit groups and waits.
+__device__ __forceinline__ void cp16(void *dst, const void *src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp4(void *dst, const void *src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void cp16s(unsigned dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp4s(unsigned dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// c + lo16(a) * lo16(b) and c + hi16(a) * hi16(b) with 16-bit operands of
+// type ACT (1 = bf16, 0 = fp16) and an fp32 accumulator.
+template <int ACT>
+__device__ __forceinline__ float fma_lo16(uint32_t a, uint32_t b, float c) {
+  float d;
+  if (ACT == 1)
+    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.bf16 %0, al, bl, %3;}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  else
+    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.f16 %0, al, bl, %3;}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+template <int ACT>
+__device__ __forceinline__ float fma_hi16(uint32_t a, uint32_t b, float c) {
+  float d;
+  if (ACT == 1)
+    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.bf16 %0, ah, bh, %3;}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  else
+    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.f16 %0, ah, bh, %3;}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
 }  // namespace rv

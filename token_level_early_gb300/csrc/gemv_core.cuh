@@ -63,31 +63,6 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t m, uint32_t
   return d;
 }
 
-// c + lo16(a) * lo16(b) and c + hi16(a) * hi16(b) with 16-bit operands of
-// type ACT (1 = bf16, 0 = fp16) and an fp32 accumulator.
-template <int ACT>
-__device__ __forceinline__ float fma_lo16(uint32_t a, uint32_t b, float c) {
-  float d;
-  if (ACT == 1)
-    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.bf16 %0, al, bl, %3;}"
-        : "=f"(d) : "r"(a), "r"(b), "f"(c));
-  else
-    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.f16 %0, al, bl, %3;}"
-        : "=f"(d) : "r"(a), "r"(b), "f"(c));
-  return d;
-}
-template <int ACT>
-__device__ __forceinline__ float fma_hi16(uint32_t a, uint32_t b, float c) {
-  float d;
-  if (ACT == 1)
-    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.bf16 %0, ah, bh, %3;}"
-        : "=f"(d) : "r"(a), "r"(b), "f"(c));
-  else
-    asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; fma.rn.f32.f16 %0, ah, bh, %3;}"
-        : "=f"(d) : "r"(a), "r"(b), "f"(c));
-  return d;
-}
-
 // Code extraction constants (mask, OR-ed bits) by activation type.
 template <int ACT>
 struct CodeBits {
@@ -212,18 +187,6 @@ __host__ __device__ __forceinline__ size_t smem_bytes(const Geo &g, int nwarp) {
   return sizeof(float) * (x_floats(g) + 256) + (size_t)nwarp * NST * STAGE;
 }
 
-__device__ __forceinline__ void cp16(void *dst, const void *src) {
-  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp4(void *dst, const void *src) {
-  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 // Eight consecutive activations x[k0..k0+8) (k0 a multiple of 8, all < K).
 template <int ACT, int PRO>
 __device__ __forceinline__ void load_x8(const GemvArgs &a, int k0, float r, float *x) {
@@ -269,13 +232,6 @@ __device__ __forceinline__ void stream_rows(const GemvArgs &a, const Geo &g, int
   is.off2 = (uint32_t)rows[2] * stride;
   is.soff0 = (uint32_t)rows[0] * (uint32_t)g.G;
   is.soff2 = (uint32_t)rows[2] * (uint32_t)g.G;
-}
-
-__device__ __forceinline__ void cp16s(unsigned dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp4s(unsigned dst, const void *src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
 // Copy the next item of the stream into `stage` (one commit group per call,

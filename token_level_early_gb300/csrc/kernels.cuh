@@ -71,6 +71,8 @@ struct AttnArgs {
   unsigned *counter;   // [B][Hkv]
 };
 cudaError_t launch_attn_decode(const AttnArgs &a, int B, cudaStream_t s, int pdl = 0);
+// Largest cluster size (power of two <= 16) launch_attn_decode can use; 0 if none.
+int attn_dec_max_cluster(int hd, int grp, int act);
 
 // Causal attention for token rows of the general path: row m of the list
 // attends to positions 0..pos(m) of its sequence.
