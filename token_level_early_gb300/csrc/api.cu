@@ -228,11 +228,19 @@ int enqueue_step_b1(rv_model *m, cudaStream_t s) {
     a.rope_cs = m->rope_cs;
     a.partials = m->partials;
 
-    // attention in: RMSNorm -> QKV -> RoPE -> K/V append
+    // exit decision of layer l (1-based) -> RMSNorm -> QKV -> RoPE -> K/V append
     a.m = make_mat(m, ly, MAT_QKV);
     a.units = m->qkv_n / 2;
     a.h = hin; a.gamma = ly.attn_norm; a.out_vec = m->qbuf;
+    if (l > 0) {
+      a.h_prev = m->hbuf[(l - 1) & 1];
+      a.decide_layer1 = l;
+      a.dbg_s = m->debug ? m->dbg_s + (size_t)(l - 1) * B : nullptr;
+    }
     RV_CK(launch_gemv_b1(m->act, PRO_NORM, EPI_QKV, a, gemv_grid(m, a.units), s, 1));
+    a.h_prev = nullptr;
+    a.decide_layer1 = 0;
+    a.dbg_s = nullptr;
 
     AttnArgs at{};
     at.kv = m->kv; at.layer = l; at.H = m->H; at.Hkv = m->Hkv; at.hd = m->hd; at.act = m->act;
@@ -252,21 +260,25 @@ int enqueue_step_b1(rv_model *m, cudaStream_t s) {
     a.h = m->hmid; a.gamma = ly.mlp_norm; a.out_vec = m->abuf;
     RV_CK(launch_gemv_b1(m->act, PRO_NORM, EPI_SWIGLU, a, gemv_grid(m, a.units), s, 1));
 
-    // down projection + residual + s(l) + exit decision
+    // down projection + residual (its exit decision is made by the next kernel)
     a.m = make_mat(m, ly, MAT_D);
     a.units = m->d;
     a.vec = m->abuf; a.h_base = m->hmid; a.h_in = hin; a.h_out = hout;
-    a.counter = m->counters + l;
     a.dbg_h = m->debug ? m->dbg_h + (size_t)(l + 1) * B * m->d : nullptr;
-    a.dbg_s = m->debug ? m->dbg_s + (size_t)l * B : nullptr;
     RV_CK(launch_gemv_b1(m->act, PRO_VEC, EPI_DOWN, a, gemv_grid(m, a.units), s, 1));
   }
-  // final RMSNorm + LM head + greedy argmax
+  // (s(L) for the debug dump) final RMSNorm + LM head + greedy argmax
   GemvArgs a{};
   a.st = m->st;
+  a.L = L;
   a.m.w = m->lm_head; a.m.N = m->V; a.m.K = m->d;
   a.units = m->V;
   a.h = m->hbuf[L & 1]; a.gamma = m->final_norm; a.eps = m->c.rms_eps;
+  if (m->debug) {  // no exit after the last layer: only the dump needs s(L)
+    a.h_prev = m->hbuf[(L - 1) & 1];
+    a.decide_layer1 = L;
+    a.dbg_s = m->dbg_s + (size_t)(L - 1) * B;
+  }
   a.partials = m->partials;
   a.counter = m->counters + L;
   a.dbg_logits = m->debug ? m->dbg_logits : nullptr;

@@ -121,6 +121,13 @@ struct KVGeom {
   }
 };
 
+// Relaxed gpu-scope load (a value another kernel may be updating).
+__device__ __forceinline__ int ld_relaxed_i32(const int32_t *p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // cp.async: 16- and 4-byte global -> shared copies, commit groups and waits.
 __device__ __forceinline__ void cp16(void *dst, const void *src) {
   const unsigned d = (unsigned)__cvta_generic_to_shared(dst);

@@ -32,42 +32,44 @@ __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
   float *scratch = smem + x_floats(g);
   char *ring = reinterpret_cast<char *>(scratch + 256) + (size_t)warp * NST * STAGE;
 
-  // In a PDL chain the route flag is final before this kernel starts for
-  // every GEMV but QKV (it was written at least two kernels earlier): those
-  // start streaming their first weight chunks while the predecessor drains.
-  // QKV's route comes from its direct predecessor, so it waits first.
-  int river;
-  if (EPI == EPI_QKV) {
-    pdl_wait();
-    river = a.st.route[0];
-  } else {
-    river = (EPI == EPI_LOGITS) ? 0 : a.st.route[0];
-  }
-  ItemStream is = gemv_begin<NW, EPI>(a, river, ring, blockIdx.x, gridDim.x);
-  if (EPI != EPI_QKV) pdl_wait();
-  pdl_trigger();
-  PhaseOut o = gemv_run<NW, ACT, PRO, EPI>(a, river, smem, scratch, ring, is, blockIdx.x, gridDim.x);
+  // The route a GEMV streams is final before the kernel starts, except for
+  // the QKV kernel, which itself makes the exit decision of the layer before
+  // (from h_prev and h, available only after the wait).  QKV starts streaming
+  // the matrices of the current route and re-streams in the one layer per
+  // token where the decision flips it.  Every block reaches the same
+  // decision (same sums in the same order); block 0 records it.  Another
+  // block may already see block 0's update when it reads the route: the
+  // update only ever says "river", which that block then decides as well.
   float *bsum = scratch + 128;
+  int river = (EPI == EPI_LOGITS) ? 0 : ld_relaxed_i32(a.st.route);
+  ItemStream is = gemv_begin<NW, EPI>(a, river, ring, blockIdx.x, gridDim.x);
+  pdl_wait();
+  pdl_trigger();
+  if ((EPI == EPI_QKV || EPI == EPI_LOGITS) && a.decide_layer1 > 0) {
+    float dot = 0.f, n1 = 0.f, n2 = 0.f;
+    for (int i = tid * 4; i < a.m.K; i += blockDim.x * 4) {
+      const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.h_prev + i));
+      const float4 y = __ldcg(reinterpret_cast<const float4 *>(a.h + i));
+      dot = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, dot))));
+      n1 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, n1))));
+      n2 = fmaf(y.x, y.x, fmaf(y.y, y.y, fmaf(y.z, y.z, fmaf(y.w, y.w, n2))));
+    }
+    dot = block_sum(dot, bsum);
+    n1 = block_sum(n1, bsum + 32);
+    n2 = block_sum(n2, bsum + 64);
+    const int route_now = (EPI == EPI_LOGITS) ? a.st.route[0] : river;
+    const Decision dc = decide(a.st, 0, route_now, a.decide_layer1, a.L, dot, n1, n2);
+    if (blockIdx.x == 0 && tid == 0) commit_decision(a.st, 0, a.decide_layer1, dc, a.dbg_s);
+    if (EPI == EPI_QKV && dc.route != river) {
+      cp_wait<0>();  // drop the speculative items, then stream the river copy
+      river = dc.route;
+      is = gemv_begin<NW, EPI>(a, river, ring, blockIdx.x, gridDim.x);
+    }
+  }
+  PhaseOut o = gemv_run<NW, ACT, PRO, EPI>(a, river, smem, scratch, ring, is, blockIdx.x, gridDim.x);
 
   if (EPI == EPI_DOWN) {
-    const float p_dot = block_sum(o.p_dot, bsum), p_n1 = block_sum(o.p_n1, bsum + 32),
-                p_n2 = block_sum(o.p_n2, bsum + 64);
-    if (tid == 0) {
-      a.partials[blockIdx.x * 3 + 0] = p_dot;
-      a.partials[blockIdx.x * 3 + 1] = p_n1;
-      a.partials[blockIdx.x * 3 + 2] = p_n2;
-    }
-    if (!last_block(a.counter)) return;
-    float t0 = 0.f, t1 = 0.f, t2 = 0.f;
-    for (int i = tid; i < (int)gridDim.x; i += blockDim.x) {
-      t0 += a.partials[i * 3 + 0];
-      t1 += a.partials[i * 3 + 1];
-      t2 += a.partials[i * 3 + 2];
-    }
-    t0 = block_sum(t0, bsum);
-    t1 = block_sum(t1, bsum + 32);
-    t2 = block_sum(t2, bsum + 64);
-    if (tid == 0) decide_row(a.st, 0, a.layer + 1, a.L, t0, t1, t2, a.dbg_s);
+    (void)o;  // the next QKV (or the LM head) makes this layer's exit decision
   } else if (EPI == EPI_LOGITS) {
     // block argmax (lowest index on ties)
     __shared__ float bv[NW * 32];

@@ -30,31 +30,52 @@ struct GemvArgs {
   float *partials;
   unsigned *counter;
   float *dbg_h;       // EPI_DOWN: hidden dump for this layer (row 0) or NULL
-  float *dbg_s;       // EPI_DOWN: s dump for this layer or NULL
+  float *dbg_s;       // s dump of the decided layer or NULL
+  // batch-1 chain, EPI_QKV / EPI_LOGITS: the exit decision of layer
+  // decide_layer1 (1-based; 0 = none), from its input h_prev and output h
+  const float *h_prev;
+  int decide_layer1;
   float *dbg_logits;  // EPI_LOGITS: logits dump or NULL
   StepState st;
 };
 
 // Exit decision for row b after layer layer1 (1-based) from the three sums
-// sum(h_in*h_out), sum(h_in^2), sum(h_out^2).  One thread calls it.
-// s = dot / max(|h_in| |h_out|, 1e-8); strict s > tau (aitrends.kr).
-__device__ __forceinline__ void decide_row(const StepState &st, int b, int layer1, int L, float dot, float n1,
-                                           float n2, float *dbg_s) {
-  if (st.route[b] != 0) {
-    if (dbg_s) dbg_s[b] = __int_as_float(0x7fc00000);
-    return;
-  }
+// sum(h_in*h_out), sum(h_in^2), sum(h_out^2), for a row whose route before
+// the decision is route_now.  s = dot / max(|h_in| |h_out|, 1e-8); strict
+// s > tau (aitrends.kr); river rows do not evaluate s (NaN).
+struct Decision {
+  int route;
+  bool exited;
+  float s;
+};
+__device__ __forceinline__ Decision decide(const StepState &st, int b, int route_now, int layer1, int L, float dot,
+                                           float n1, float n2) {
+  Decision d{route_now, false, __int_as_float(0x7fc00000)};
+  if (route_now != 0) return d;
   const float den = fmaxf(sqrtf(n1) * sqrtf(n2), 1e-8f);
-  const float s = dot / den;
-  if (dbg_s) dbg_s[b] = s;
+  d.s = dot / den;
   if (*st.mode == 1) {
     int f = st.forced[b];
     if (f < 0 || f > L) f = L;
-    if (layer1 == f && layer1 < L) { st.route[b] = 1; st.exit_layer[b] = layer1; }
-  } else if (layer1 >= *st.entry && layer1 <= L - 1 && s > *st.tau) {
+    d.exited = layer1 == f && layer1 < L;
+  } else {
+    d.exited = layer1 >= *st.entry && layer1 <= L - 1 && d.s > *st.tau;
+  }
+  if (d.exited) d.route = 1;
+  return d;
+}
+// Record a decision in the step state (one thread).
+__device__ __forceinline__ void commit_decision(const StepState &st, int b, int layer1, const Decision &d,
+                                                float *dbg_s) {
+  if (dbg_s) dbg_s[b] = d.s;
+  if (d.exited) {
     st.route[b] = 1;
     st.exit_layer[b] = layer1;
   }
+}
+__device__ __forceinline__ void decide_row(const StepState &st, int b, int layer1, int L, float dot, float n1,
+                                           float n2, float *dbg_s) {
+  commit_decision(st, b, layer1, decide(st, b, st.route[b], layer1, L, dot, n1, n2), dbg_s);
 }
 
 cudaError_t launch_gemv_b1(int act, int pro, int epi, const GemvArgs &a, int grid, cudaStream_t s, int pdl = 0);
