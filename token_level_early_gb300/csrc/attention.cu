@@ -366,6 +366,213 @@ int attn_dec_max_cluster(int hd, int grp, int act) {
   return 0;
 }
 
+// ---- prefill: causal flash attention on the tensor pipe --------------------
+// Block: 16 consecutive tokens of sequence b x the GRP query heads of kv head
+// g (one warp per head), so each K/V tile serves GRP heads.  K/V tiles of 64
+// positions stream through a double-buffered cp.async ring, rows padded by 16
+// bytes so ldmatrix reads are conflict-free; positions past the causal bound
+// are zero-filled.  S = Q K^T and O += P V run as mma.sync m16n8k16 with
+// 16-bit operands and fp32 accumulators; the online softmax is fp32, and P
+// enters the P V product as two 16-bit terms, P = hi + lo with hi = round16(P)
+// and lo = round16(P - hi), so the product keeps about 16 significant bits
+// of P.  Blocks are issued longest-first (last tokens first).
+constexpr int PQ = 16;  // tokens per block (one m16 tile per warp)
+constexpr int PK = 64;  // key positions per tile
+
+template <int HD>
+struct PreTile {
+  static constexpr int ROW = HD * 2 + 16;
+  static constexpr int KV = PK * ROW;
+  static constexpr int BYTES = 2 * KV;
+};
+
+__device__ __forceinline__ void cp16z(unsigned dst, const void *src, bool valid) {
+  const int n = valid ? 16 : 0;  // 0: zero-fill, nothing read
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t *r, unsigned addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t *r, unsigned addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+template <int ACT>
+__device__ __forceinline__ void mma16816(float *d, const uint32_t *a, const uint32_t *b) {
+  if (ACT == 1)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+template <int HD, int GRP, int ACT>
+__global__ void __launch_bounds__(GRP * 32) k_attn_prefill(AttnRowsArgs a, int T) {
+  using PT = PreTile<HD>;
+  constexpr int NT = GRP * 32, KS = HD / 16, DT = HD / 8, PR = HD / 8;
+  extern __shared__ __align__(16) unsigned char sm[];
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = g * GRP + warp, gq = lane >> 2, tq = lane & 3;
+  const int base = a.base ? a.base[b] : 0;
+  const int t0 = (gridDim.x - 1 - blockIdx.x) * PQ;  // first token of the block
+  const int kend = base + min(T, t0 + PQ);           // keys [0, kend)
+  const int ntile = (kend + PK - 1) / PK;
+  const uint16_t *Kb = a.kv.base + a.kv.idx(a.layer, 0, b, g, 0);
+  const uint16_t *Vb = a.kv.base + a.kv.idx(a.layer, 1, b, g, 0);
+  const unsigned sb = (unsigned)__cvta_generic_to_shared(sm);
+
+  auto issue = [&](int tile, int slot) {
+    if (tile < ntile) {
+      const int j0 = tile * PK;
+      const unsigned st = sb + slot * PT::BYTES;
+      for (int v = tid; v < 2 * PK * PR; v += NT) {
+        const int kv = v >= PK * PR, rem = v - kv * PK * PR, j = rem / PR, c = rem - j * PR;
+        const bool ok = j0 + j < kend;
+        const uint16_t *src = (kv ? Vb : Kb) + (size_t)(ok ? j0 + j : 0) * HD + c * 8;
+        cp16z(st + kv * PT::KV + j * PT::ROW + c * 16, src, ok);
+      }
+    }
+    cp_commit();
+  };
+  issue(0, 0);
+
+  // Q fragments (A operand: rows = the warp's 16 tokens, k = head dims)
+  const int r0 = t0 + gq, r1 = r0 + 8;
+  uint32_t qa[KS][4];
+  {
+    const size_t ld = (size_t)a.H * HD;
+    const float *q0 = a.q + ((size_t)b * T + r0) * ld + (size_t)h * HD;
+    const float *q1 = a.q + ((size_t)b * T + r1) * ld + (size_t)h * HD;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int d = 16 * ks + 2 * tq;
+      float2 x00 = make_float2(0.f, 0.f), x10 = x00, x01 = x00, x11 = x00;
+      if (r0 < T) { x00 = *reinterpret_cast<const float2 *>(q0 + d); x01 = *reinterpret_cast<const float2 *>(q0 + d + 8); }
+      if (r1 < T) { x10 = *reinterpret_cast<const float2 *>(q1 + d); x11 = *reinterpret_cast<const float2 *>(q1 + d + 8); }
+      qa[ks][0] = pack_act2(x00.x, x00.y, ACT);
+      qa[ks][1] = pack_act2(x10.x, x10.y, ACT);
+      qa[ks][2] = pack_act2(x01.x, x01.y, ACT);
+      qa[ks][3] = pack_act2(x11.x, x11.y, ACT);
+    }
+  }
+  const int p0 = base + r0, p1 = base + r1;  // positions of the thread's two rows
+  const float sl2 = 1.4426950408889634f / sqrtf((float)HD);  // softmax in base 2
+  float o[DT][4];
+#pragma unroll
+  for (int i = 0; i < DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  for (int tile = 0; tile < ntile; ++tile) {
+    cp_wait<0>();
+    __syncthreads();  // tile in; every warp is done with the other slot
+    issue(tile + 1, (tile + 1) & 1);
+    const unsigned kt = sb + (tile & 1) * PT::BYTES, vt = kt + PT::KV;
+    const int j0 = tile * PK;
+    float sc[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    const int mi = lane >> 3;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t kb[4];
+        ldsm_x4(kb, kt + (16 * np + (mi >> 1) * 8 + (lane & 7)) * PT::ROW + (16 * ks + (mi & 1) * 8) * 2);
+        mma16816<ACT>(sc[2 * np], qa[ks], kb);
+        mma16816<ACT>(sc[2 * np + 1], qa[ks], kb + 2);
+      }
+    // scale, causal mask, online softmax (rows p0: elements 0,1; p1: 2,3)
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int k0 = j0 + nt * 8 + 2 * tq;
+      sc[nt][0] = k0 <= p0 ? sc[nt][0] * sl2 : -INFINITY;
+      sc[nt][1] = k0 + 1 <= p0 ? sc[nt][1] * sl2 : -INFINITY;
+      sc[nt][2] = k0 <= p1 ? sc[nt][2] * sl2 : -INFINITY;
+      sc[nt][3] = k0 + 1 <= p1 ? sc[nt][3] * sl2 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);  // finite: key 0 is in the first tile
+    const float c0 = exp2f(m0 - n0), c1 = exp2f(m1 - n1);
+    float s0 = 0.f, s1 = 0.f;
+    uint32_t pa[4][4], pl[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const float e0 = exp2f(sc[nt][0] - n0), e1 = exp2f(sc[nt][1] - n0);
+      const float e2 = exp2f(sc[nt][2] - n1), e3 = exp2f(sc[nt][3] - n1);
+      s0 += e0 + e1;
+      s1 += e2 + e3;
+      const float h0 = round_act(e0, ACT), h1 = round_act(e1, ACT), h2 = round_act(e2, ACT), h3 = round_act(e3, ACT);
+      pa[nt >> 1][(nt & 1) * 2] = pack_act2(h0, h1, ACT);
+      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_act2(h2, h3, ACT);
+      pl[nt >> 1][(nt & 1) * 2] = pack_act2(e0 - h0, e1 - h1, ACT);
+      pl[nt >> 1][(nt & 1) * 2 + 1] = pack_act2(e2 - h2, e3 - h3, ACT);
+    }
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    l0 = l0 * c0 + s0;
+    l1 = l1 * c1 + s1;
+    m0 = n0;
+    m1 = n1;
+#pragma unroll
+    for (int i = 0; i < DT; ++i) {
+      o[i][0] *= c0; o[i][1] *= c0; o[i][2] *= c1; o[i][3] *= c1;
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int dp = 0; dp < DT / 2; ++dp) {
+        uint32_t vb[4];
+        ldsm_x4_t(vb, vt + (16 * kk + (mi & 1) * 8 + (lane & 7)) * PT::ROW + (16 * dp + (mi >> 1) * 8) * 2);
+        mma16816<ACT>(o[2 * dp], pa[kk], vb);
+        mma16816<ACT>(o[2 * dp + 1], pa[kk], vb + 2);
+        mma16816<ACT>(o[2 * dp], pl[kk], vb);
+        mma16816<ACT>(o[2 * dp + 1], pl[kk], vb + 2);
+      }
+  }
+  cp_wait<0>();
+
+  const size_t ld = (size_t)a.H * HD;
+  const float i0 = 1.0f / l0, i1 = 1.0f / l1;
+#pragma unroll
+  for (int i = 0; i < DT; ++i) {
+    const int d = 8 * i + 2 * tq;
+    if (r0 < T)
+      *reinterpret_cast<float2 *>(a.o + ((size_t)b * T + r0) * ld + (size_t)h * HD + d) =
+          make_float2(round_act(o[i][0] * i0, ACT), round_act(o[i][1] * i0, ACT));
+    if (r1 < T)
+      *reinterpret_cast<float2 *>(a.o + ((size_t)b * T + r1) * ld + (size_t)h * HD + d) =
+          make_float2(round_act(o[i][2] * i1, ACT), round_act(o[i][3] * i1, ACT));
+  }
+}
+
+template <int HD, int GRP, int ACT>
+static cudaError_t launch_pre(const AttnRowsArgs &a, int B, int T, cudaStream_t s) {
+  auto fn = k_attn_prefill<HD, GRP, ACT>;
+  const int smem = 2 * PreTile<HD>::BYTES;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((T + PQ - 1) / PQ, a.Hkv, B);
+  fn<<<grid, GRP * 32, smem, s>>>(a, T);
+  return cudaGetLastError();
+}
+
 template <int HD, int GRP>
 static cudaError_t launch_hg(const AttnArgs &a, int T_per_row, const int32_t *base, int rows, cudaStream_t s,
                              int pdl) {
@@ -398,8 +605,20 @@ cudaError_t launch_attn_decode(const AttnArgs &a, int B, cudaStream_t s, int pdl
   return cudaErrorInvalidValue;
 }
 
-// Prefill / general rows: T tokens per sequence starting at base (NULL = 0).
+// Prefill / general rows: T tokens per sequence starting at base (NULL = 0),
+// max_rows = B * T rows.  Token rows (T > 1) run the tensor-pipe flash
+// attention; the per-row kernel remains for list-driven rows.
 cudaError_t launch_attn_rows(const AttnRowsArgs &r, int max_rows, cudaStream_t s) {
+  const int T = r.tokens_per_row, grp = r.H / r.Hkv;
+  if (T > 1 && !r.list && max_rows % T == 0) {
+    const int B = max_rows / T;
+#define RV_PL(HD_, G_)                                                                    \
+    if (r.hd == HD_ && grp == G_)                                                         \
+      return r.act == 1 ? launch_pre<HD_, G_, 1>(r, B, T, s) : launch_pre<HD_, G_, 0>(r, B, T, s);
+    RV_PL(64, 1) RV_PL(64, 2) RV_PL(64, 4) RV_PL(64, 8)
+    RV_PL(128, 1) RV_PL(128, 2) RV_PL(128, 4) RV_PL(128, 8)
+#undef RV_PL
+  }
   AttnArgs a;
   a.kv = r.kv;
   a.layer = r.layer; a.H = r.H; a.Hkv = r.Hkv; a.hd = r.hd; a.act = r.act;
