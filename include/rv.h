@@ -49,7 +49,7 @@ extern "C" {
 #define RV_ECUDA (-3)      /* a CUDA runtime call failed */
 #define RV_ECAPACITY (-4)  /* a row's KV cache is full (len == max_seq); nothing changed */
 #define RV_ESTATE (-5)     /* call out of order, e.g. tau-rule decode before rv_quantize_river */
-#define RV_ETIMEOUT (-6)   /* reserved: a bounded device wait gave up */
+#define RV_ETIMEOUT (-6)   /* a bounded device wait gave up (persistent engine grid barrier) */
 
 /* Projection ids of a decoder layer (for rv_export_river). */
 #define RV_PROJ_Q 0

@@ -755,6 +755,14 @@ static int validate_step(rv_model *m, int B, const int32_t *forced_host, bool fo
   return RV_OK;
 }
 
+// Device error flags -> status: bit 3 = a persistent-kernel grid barrier
+// gave up waiting; the other bits flag invalid inputs (token, forced exit,
+// quantization).
+static int device_status(int32_t err) {
+  if (err & 8) return fail(RV_ETIMEOUT, "a grid barrier of the persistent decode kernel timed out (0x%x)", err);
+  return fail(RV_EINVAL, "device flagged an invalid input (0x%x)", err);
+}
+
 int rv_decode_step(rv_model *m, const int32_t *tokens, int B, float tau, const int32_t *forced_exit,
                    int32_t *next_ids, int32_t *exit_layer) {
   g_err.clear();
@@ -775,7 +783,7 @@ int rv_decode_step(rv_model *m, const int32_t *tokens, int B, float tau, const i
   int32_t *out = pin_out(m);
   RV_CK(cudaMemcpyAsync(out, m->st.next_ids, sizeof(int32_t) * m->out_words, cudaMemcpyDeviceToHost, m->stream));
   RV_CK(cudaStreamSynchronize(m->stream));
-  if (out[2 * m->Bmax]) return fail(RV_EINVAL, "device flagged an invalid input (0x%x)", out[2 * m->Bmax]);
+  if (out[2 * m->Bmax]) return device_status(out[2 * m->Bmax]);
   memcpy(next_ids, out, sizeof(int32_t) * B);
   memcpy(exit_layer, out + m->Bmax, sizeof(int32_t) * B);
   for (int b = 0; b < B; ++b) m->h_len[b] += 1;
@@ -811,7 +819,7 @@ int rv_sync_status(rv_model *m) {
   int32_t err = 0;
   RV_CK(cudaMemcpyAsync(&err, m->st.err, sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
   RV_CK(cudaStreamSynchronize(m->stream));
-  if (err) return fail(RV_EINVAL, "device flagged an invalid input (0x%x)", err);
+  if (err) return device_status(err);
   return RV_OK;
 }
 
@@ -859,7 +867,7 @@ int rv_prefill(rv_model *m, const int32_t *tokens, int B, int T0, float tau, int
   int32_t *out = pin_out(m);
   RV_CK(cudaMemcpyAsync(out, m->st.next_ids, sizeof(int32_t) * m->out_words, cudaMemcpyDeviceToHost, s));
   RV_CK(cudaStreamSynchronize(s));
-  if (out[2 * m->Bmax]) return fail(RV_EINVAL, "device flagged an invalid input (0x%x)", out[2 * m->Bmax]);
+  if (out[2 * m->Bmax]) return device_status(out[2 * m->Bmax]);
   memcpy(next_ids, out, sizeof(int32_t) * B);
   memcpy(exit_layer, out + m->Bmax, sizeof(int32_t) * B);
   for (int b = 0; b < B; ++b) m->h_len[b] = T0;
