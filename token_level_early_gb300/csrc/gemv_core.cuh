@@ -10,6 +10,11 @@
 // transpose-reduce and, for S > 1, across the splits through shared memory;
 // the epilogue runs in the warp that owns the quad.
 //
+// Activations are staged as 16-bit values (exact: every GEMV input is
+// rounded to the model's 16-bit type) and multiplied by mixed-precision FMAs
+// (16-bit operands, fp32 accumulator, exact products).  16-bit path: the two
+// halves of a weight word against the two halves of an activation word.
+//
 // int4 inner loop.  One LOP3 turns two codes of a word into a pair of 16-bit
 // floats with the code in the low mantissa bits: bf16 128 + q (mask the
 // nibbles at bits 0..3 and 16..19, OR in the bits of 128.0), or fp16 1 + q/16
@@ -29,31 +34,6 @@ namespace rv {
 constexpr int CH4 = 1024;  // int4 chunk: 32 lanes x 32 codes
 constexpr int CH16 = 256;  // 16-bit chunk: 32 lanes x 8 values
 
-typedef unsigned long long u64;
-
-// 128-bit streaming load that does not allocate in L1 (weights are read once).
-__device__ __forceinline__ uint4 ld_stream(const void *p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ u64 pack2(float lo, float hi) {
-  return ((u64)__float_as_uint(hi) << 32) | (u64)__float_as_uint(lo);
-}
-
-__device__ __forceinline__ float sum2(u64 v) {
-  return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
-}
-
-// d = a * b + c on two fp32 lanes at once.
-__device__ __forceinline__ u64 ffma2(u64 a, u64 b, u64 c) {
-  u64 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
 
 // d = (a & m) | c in one instruction (the compiler splits the two-constant
 // form into two).
@@ -90,19 +70,6 @@ __device__ __forceinline__ void word_mix(uint32_t w, const uint32_t *xr, float &
   a0 = fma_lo16<ACT>(c1, xr[1], a0); a1 = fma_hi16<ACT>(c1, xr[1], a1);
   a0 = fma_lo16<ACT>(c2, xr[2], a0); a1 = fma_hi16<ACT>(c2, xr[2], a1);
   a0 = fma_lo16<ACT>(c3, xr[3], a0); a1 = fma_hi16<ACT>(c3, xr[3], a1);
-}
-
-// Two 16-bit weights of a word times their activations (packed fp32 FMA).
-template <int ACT>
-__device__ __forceinline__ u64 pair16_fma(uint32_t w, u64 x, u64 acc) {
-  u64 f;
-  if (ACT == 1) {
-    f = ((u64)(w & 0xFFFF0000u) << 32) | (u64)(w << 16);
-  } else {
-    const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&w));
-    f = pack2(v.x, v.y);
-  }
-  return ffma2(f, x, acc);
 }
 
 // Rows of quad qd by epilogue; pairs (0,2) and (1,3) stay together where the
@@ -180,7 +147,7 @@ constexpr int STAGE = STAGE_W + STAGE_S;
 // 256 floats of reduction scratch, then the warps' staging rings.
 __host__ __device__ __forceinline__ size_t x_floats(const Geo &g) {
   const size_t river = (size_t)g.nk4 * (4 * 32 * 4 + 32);
-  const size_t b16 = (size_t)g.nk16 * (2 * 32 * 4);
+  const size_t b16 = (size_t)g.nk16 * (32 * 4);
   return river > b16 ? river : b16;
 }
 __host__ __device__ __forceinline__ size_t smem_bytes(const Geo &g, int nwarp) {
@@ -368,13 +335,15 @@ __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float
       xsum[c * 32 + ln] = X;
     }
   } else {
-    float4 *xb = reinterpret_cast<float4 *>(xs);  // [nk][2][32]
+    uint4 *xb = reinterpret_cast<uint4 *>(xs);  // [nk][32]: the lane's 8 activations as 16-bit pairs
     for (int t = tid; t < nk * 32; t += blockDim.x) {
       const int c = t >> 5, ln = t & 31, base = c * CH16 + ln * 8;
       float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if (base < g.K) load_x8<ACT, PRO>(a, base, rs, x);
-      xb[(c * 2) * 32 + ln] = make_float4(x[0], x[1], x[2], x[3]);
-      xb[(c * 2 + 1) * 32 + ln] = make_float4(x[4], x[5], x[6], x[7]);
+      xb[c * 32 + ln] = make_uint4((uint32_t)f_to_act(x[0], ACT) | ((uint32_t)f_to_act(x[1], ACT) << 16),
+                                   (uint32_t)f_to_act(x[2], ACT) | ((uint32_t)f_to_act(x[3], ACT) << 16),
+                                   (uint32_t)f_to_act(x[4], ACT) | ((uint32_t)f_to_act(x[5], ACT) << 16),
+                                   (uint32_t)f_to_act(x[6], ACT) | ((uint32_t)f_to_act(x[7], ACT) << 16));
     }
   }
   __syncthreads();
@@ -393,7 +362,7 @@ __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float
     int rows[4] = {0, 0, 0, 0};
     if (qd < nquads) {
       quad_rows<EPI>(a, qd, rows);
-      u64 acc[4] = {0ull, 0ull, 0ull, 0ull};
+      float al[4] = {0.f, 0.f, 0.f, 0.f}, ah[4] = {0.f, 0.f, 0.f, 0.f};
       for (int c = sp; c < nk; c += S, ++t) {
         cp_wait<NST - 2>();  // this lane's copies of item t have landed
         issue_item<EPI>(a, g, river, rg, nquads, nk, S, sp, p.lane_g, is, ring + ((t + NST - 1) & (NST - 1)) * STAGE,
@@ -427,22 +396,24 @@ __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float
         } else {
           const int k0 = c * CH16 + lane * 8;
           if (k0 >= g.K) continue;
-          const float4 *xb = reinterpret_cast<const float4 *>(xs);
-          const float4 f0 = xb[(c * 2) * 32 + lane], f1 = xb[(c * 2 + 1) * 32 + lane];
-          const u64 x0 = pack2(f0.x, f0.y), x1 = pack2(f0.z, f0.w), x2 = pack2(f1.x, f1.y), x3 = pack2(f1.z, f1.w);
+          const uint4 xv = reinterpret_cast<const uint4 *>(xs)[c * 32 + lane];
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const uint4 w = sw[r * 32 + lane];
-            acc[r] = pair16_fma<ACT>(w.x, x0, acc[r]);
-            acc[r] = pair16_fma<ACT>(w.y, x1, acc[r]);
-            acc[r] = pair16_fma<ACT>(w.z, x2, acc[r]);
-            acc[r] = pair16_fma<ACT>(w.w, x3, acc[r]);
+            al[r] = fma_lo16<ACT>(w.x, xv.x, al[r]);
+            ah[r] = fma_hi16<ACT>(w.x, xv.x, ah[r]);
+            al[r] = fma_lo16<ACT>(w.y, xv.y, al[r]);
+            ah[r] = fma_hi16<ACT>(w.y, xv.y, ah[r]);
+            al[r] = fma_lo16<ACT>(w.z, xv.z, al[r]);
+            ah[r] = fma_hi16<ACT>(w.z, xv.z, ah[r]);
+            al[r] = fma_lo16<ACT>(w.w, xv.w, al[r]);
+            ah[r] = fma_hi16<ACT>(w.w, xv.w, ah[r]);
           }
         }
       }
       if (!river) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) v[r] = sum2(acc[r]);
+        for (int r = 0; r < 4; ++r) v[r] = al[r] + ah[r];
       }
     }
     // row r of the quad ends in lane 8 r of every warp of the quad's group
