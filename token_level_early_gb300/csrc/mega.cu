@@ -3,22 +3,26 @@
 // pick) in one cooperative launch with one resident block per SM.
 //
 // Phases of layer l, separated by grid barriers:
-//   QKV  : RMSNorm(h) -> W_qkv (bf16 or int4) -> RoPE -> K/V into slot (l, 0, p)
-//   ATTN : split-KV GQA attention over positions 0..p (one task per block)
+//   QKV  : exit decision of layer l - 1 (every block, from h(l-1) and h(l)),
+//          RMSNorm(h) -> W_qkv (bf16 or int4) -> RoPE -> K/V into slot (l, 0, p)
+//   ATTN : split-KV GQA attention over positions 0..p (one task per block);
+//          each block starts copying its first K/V tile before the barrier
 //   COMB : merge of the splits' softmax states -> o
 //   O    : h_mid = h + W_o o
 //   GU   : RMSNorm(h_mid) -> a = silu(W_g x) * (W_u x)
-//   DOWN : h_out = h_mid + W_d a; per-block sums of h_in.h_out, |h_in|^2, |h_out|^2
-//   then every block adds the per-block sums in the same order, so all blocks
-//   take the same exit decision s(l) = cos(h_in, h_out) > tau without another
-//   barrier.  Before each barrier the warps already issue the next phase's
-//   first weight chunks into their cp.async rings, so the weight stream keeps
-//   running while blocks wait.
+//   DOWN : h_out = h_mid + W_d a
+// Every block reaches the same exit decision from the same sums in the same
+// order.  Before each barrier the warps already issue the next phase's first
+// weight chunks into their cp.async rings (QKV on the route before the
+// decision; re-streamed in the one layer per token where it flips), so the
+// weight stream keeps running while blocks wait.
 //
-// Grid barrier: an arrival counter and an epoch word in global memory; the
-// last block to arrive resets the counter and advances the epoch.  Waiting is
-// bounded: after about a second without progress a block sets error bit 8 and
-// every block leaves the kernel at its next barrier (copies drained first).
+// Grid barrier: a counter in global memory that only grows within a launch
+// (the host zeroes it before each step); a block adds 1 with release
+// semantics and polls with acquire loads until the counter reaches
+// epoch x blocks.  Waiting is bounded: after about a second without progress
+// a block sets error bit 8 and every block leaves the kernel at its next
+// barrier (copies drained first).
 //
 // Method: "River-LLM: Large Language Model Seamless Exit Based on KV Share",
 // paperlayer.ai summary section 4 (KV-Shared Exit Layer; Inference with
@@ -38,29 +42,27 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
   return v;
 }
 
+__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ bool grid_barrier(unsigned *bar, unsigned &epoch, int32_t *err) {
   __shared__ int ok;
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned target = epoch + 1;
+    epoch += 1;
+    const unsigned target = epoch * gridDim.x;
     __threadfence();
-    const unsigned prev = atomicAdd(&bar[0], 1u);
-    if (prev == gridDim.x - 1) {
-      atomicExch(&bar[0], 0u);
-      __threadfence();
-      atomicExch(&bar[1], target);
-    } else {
-      unsigned it = 0;
-      while (ld_acquire(&bar[1]) != target) {
-        if (++it > (1u << 21)) {
-          atomicOr(err, 8);
-          break;
-        }
-        __nanosleep(64);
+    red_release_add(bar, 1u);
+    unsigned it = 0;
+    while ((int)(ld_acquire(bar) - target) < 0) {
+      if (++it > (1u << 21)) {
+        atomicOr(err, 8);
+        break;
       }
+      __nanosleep(32);
     }
     __threadfence();
-    epoch = target;
     ok = (*(volatile int32_t *)err & 8) == 0;
   }
   __syncthreads();
@@ -106,77 +108,143 @@ __device__ __forceinline__ GemvArgs head_args(const MegaArgs &A) {
   return a;
 }
 
-// Split-KV attention task (kv head g, split sp of S) over positions 0..pos:
-// warps 0..GRP-1 take the GRP query heads of KV head g; every warp helps to
-// stage the K/V tile.  Publishes (o unnormalised, running max, running sum).
-template <int HD, int GRP>
-__device__ void attn_task(const MegaArgs &A, int l, int g, int sp, int S, int pos, float *tiles) {
-  float *qs = tiles;                      // [GRP][HD]
-  float *Ks = qs + GRP * HD;              // [ATILE][HD + 1]
-  float *Vs = Ks + ATILE * (HD + 1);      // [ATILE][HD]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nt = blockDim.x;
-  constexpr int PER = HD / 32;
-  const int T = pos + 1, chunk = (T + S - 1) / S, t0 = sp * chunk, t1 = min(T, t0 + chunk);
-  __syncthreads();  // a previous task of this block may still be reading the tiles
-  for (int i = threadIdx.x; i < GRP * HD; i += nt) qs[i] = __ldcg(A.q + (size_t)g * GRP * HD + i);
-  const uint16_t *Kb = A.kv.base + A.kv.idx(l, 0, 0, g, 0);
-  const uint16_t *Vb = A.kv.base + A.kv.idx(l, 1, 0, g, 0);
+// Split-KV attention.  Task t = (kv head g, split sp of S): split sp takes
+// tiles [tb, te) of the past positions 0..p-1 (tiles of ATILE positions,
+// split evenly), the last split also position p.  K/V tiles are copied by
+// cp.async into a 2-slot ring in the activation region (K rows padded by 16
+// bytes: conflict-free row-per-lane reads); warps 0..GRP-1 take the GRP query
+// heads of kv head g, scores by mixed-precision FMAs on 16-bit q and K.
+// Publishes (o unnormalised, running max, running sum) per query head.
+template <int HD>
+struct MegaTile {
+  static constexpr int KROW = HD * 2 + 16;
+  static constexpr int VROW = HD * 2;
+  static constexpr int BYTES = ATILE * (KROW + VROW);
+};
+
+__device__ __forceinline__ void split_tiles(int p, int S, int sp, int &tb, int &te) {
+  const int ntile = (p + ATILE - 1) / ATILE, per = (ntile + S - 1) / S;
+  tb = min(ntile, sp * per);
+  te = min(ntile, tb + per);
+}
+
+// Copy tile `tile` (if below te) of kv head g into ring slot `slot`; one
+// commit group per call.
+template <int HD>
+__device__ __forceinline__ void attn_issue(const MegaArgs &A, int l, int g, int tile, int te, int p, int slot,
+                                           unsigned char *ring_a) {
+  using TL = MegaTile<HD>;
+  if (tile < te) {
+    const int t0 = tile * ATILE, n = min(ATILE, p - t0);
+    const uint16_t *Kb = A.kv.base + A.kv.idx(l, 0, 0, g, 0), *Vb = A.kv.base + A.kv.idx(l, 1, 0, g, 0);
+    const unsigned st = (unsigned)__cvta_generic_to_shared(ring_a) + slot * TL::BYTES;
+    constexpr int PR = HD / 8;
+    for (int v = threadIdx.x; v < 2 * ATILE * PR; v += blockDim.x) {
+      const int kv = v >= ATILE * PR, rem = v - kv * ATILE * PR, t = rem / PR, c = rem - t * PR;
+      if (t < n)
+        cp16s(st + (kv ? ATILE * TL::KROW + t * TL::VROW : t * TL::KROW) + c * 16,
+              (kv ? Vb : Kb) + (size_t)(t0 + t) * HD + c * 8);
+    }
+  }
+  cp_commit();
+}
+
+// qs: GRP * HD / 2 words of shared memory for q as 16-bit pairs.
+template <int ACT, int HD, int GRP>
+__device__ void attn_task(const MegaArgs &A, int l, int task, int S, int p, unsigned char *ring_a,
+                          bool first_issued, uint32_t *qs) {
+  using TL = MegaTile<HD>;
+  constexpr int PER = HD / 32, PR = HD / 8;
+  const int g = task / S, sp = task - g * S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int tb, te;
+  split_tiles(p, S, sp, tb, te);
+  if (!first_issued) attn_issue<HD>(A, l, g, tb, te, p, 0, ring_a);
+  const int h = g * GRP + (warp < GRP ? warp : 0);
+  const float *qp = A.q + (size_t)h * HD;
+  // q of the GRP heads as 16-bit pairs (q is act-rounded after RoPE: exact)
+  for (int i = threadIdx.x; i < GRP * HD / 2; i += blockDim.x) {
+    const float2 v = __ldcg(reinterpret_cast<const float2 *>(A.q + (size_t)g * GRP * HD) + i);
+    qs[i] = (uint32_t)f_to_act(v.x, ACT) | ((uint32_t)f_to_act(v.y, ACT) << 16);
+  }
+  const uint4 *q4 = reinterpret_cast<const uint4 *>(qs + (warp < GRP ? warp : 0) * (HD / 2));
   const float scale = 1.0f / sqrtf((float)HD);
   float mrun = -INFINITY, lrun = 0.f, o[PER];
 #pragma unroll
   for (int r = 0; r < PER; ++r) o[r] = 0.f;
-  for (int tile = t0; tile < t1; tile += ATILE) {
-    const int n = min(ATILE, t1 - tile);
-    __syncthreads();
-    for (int v = threadIdx.x; v < n * (HD / 8); v += nt) {
-      const int t = v / (HD / 8), c = (v % (HD / 8)) * 8;
-      const uint4 kw = __ldcg(reinterpret_cast<const uint4 *>(Kb + (size_t)(tile + t) * HD + c));
-      const uint4 vw = __ldcg(reinterpret_cast<const uint4 *>(Vb + (size_t)(tile + t) * HD + c));
-      const uint16_t *kp = reinterpret_cast<const uint16_t *>(&kw);
-      const uint16_t *vp = reinterpret_cast<const uint16_t *>(&vw);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        Ks[t * (HD + 1) + c + j] = act_to_f(kp[j], A.act);
-        Vs[t * HD + c + j] = act_to_f(vp[j], A.act);
-      }
-    }
+  for (int tile = tb, it = 0; tile < te; ++tile, ++it) {
+    __syncthreads();  // every warp is done with the slot refilled next
+    attn_issue<HD>(A, l, g, tile + 1, te, p, (it + 1) & 1, ring_a);
+    cp_wait<1>();     // all but the newest group: tile `tile` (and older weight items) landed
     __syncthreads();
     if (warp < GRP) {
+      const unsigned char *tk = ring_a + (it & 1) * TL::BYTES, *tv = tk + ATILE * TL::KROW;
+      const int n = min(ATILE, p - tile * ATILE);
       float sc = -INFINITY;
       if (lane < n) {
-        float d = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < HD; ++i) d = fmaf(qs[warp * HD + i], Ks[lane * (HD + 1) + i], d);
-        sc = d * scale;
+        const uint4 *kr = reinterpret_cast<const uint4 *>(tk + lane * TL::KROW);
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < PR; ++j) {
+          const uint4 k = kr[j], q = q4[j];
+          d0 = fma_lo16<ACT>(k.x, q.x, d0);
+          d1 = fma_hi16<ACT>(k.x, q.x, d1);
+          d2 = fma_lo16<ACT>(k.y, q.y, d2);
+          d3 = fma_hi16<ACT>(k.y, q.y, d3);
+          d0 = fma_lo16<ACT>(k.z, q.z, d0);
+          d1 = fma_hi16<ACT>(k.z, q.z, d1);
+          d2 = fma_lo16<ACT>(k.w, q.w, d2);
+          d3 = fma_hi16<ACT>(k.w, q.w, d3);
+        }
+        sc = ((d0 + d1) + (d2 + d3)) * scale;
       }
-      const float mt = warp_max(sc);
-      const float mnew = fmaxf(mrun, mt);
-      const float p = lane < n ? expf(sc - mnew) : 0.f;
+      const float mnew = fmaxf(mrun, warp_max(sc));
+      const float pe = lane < n ? expf(sc - mnew) : 0.f;
       const float corr = mrun == -INFINITY ? 0.f : expf(mrun - mnew);
-      lrun = lrun * corr + warp_sum(p);
+      lrun = lrun * corr + warp_sum(pe);
 #pragma unroll
       for (int r = 0; r < PER; ++r) o[r] *= corr;
       for (int t = 0; t < n; ++t) {
-        const float pt = __shfl_sync(0xffffffffu, p, t);
+        const float pt = __shfl_sync(0xffffffffu, pe, t);
+        const uint16_t *vr = reinterpret_cast<const uint16_t *>(tv + t * TL::VROW) + lane * PER;
 #pragma unroll
-        for (int r = 0; r < PER; ++r) o[r] = fmaf(pt, Vs[t * HD + lane + 32 * r], o[r]);
+        for (int r = 0; r < PER; ++r) o[r] = fmaf(pt, act_to_f(vr[r], ACT), o[r]);
       }
       mrun = mnew;
     }
   }
   if (warp < GRP) {
-    const int h = g * GRP + warp;
+    if (sp == S - 1) {  // position p, written in the QKV phase
+      const uint16_t *kc = A.kv.base + A.kv.idx(l, 0, 0, g, p) + lane * PER;
+      const uint16_t *vc = A.kv.base + A.kv.idx(l, 1, 0, g, p) + lane * PER;
+      float d = 0.f;
+#pragma unroll
+      for (int r = 0; r < PER; ++r) d = fmaf(__ldcg(qp + lane * PER + r), act_to_f(__ldcg(kc + r), ACT), d);
+      const float sc = warp_sum(d) * scale;
+      const float mnew = fmaxf(mrun, sc);
+      const float corr = mrun == -INFINITY ? 0.f : expf(mrun - mnew), pe = expf(sc - mnew);
+      lrun = lrun * corr + pe;
+#pragma unroll
+      for (int r = 0; r < PER; ++r) o[r] = fmaf(pe, act_to_f(__ldcg(vc + r), ACT), o[r] * corr);
+      mrun = mnew;
+    }
     float *pp = A.attn_part + ((size_t)h * S + sp) * (HD + 2);
 #pragma unroll
-    for (int r = 0; r < PER; ++r) pp[lane + 32 * r] = o[r];
-    if (lane == 0) { pp[HD] = mrun; pp[HD + 1] = lrun; }
+    for (int r = 0; r < PER; ++r) pp[lane * PER + r] = o[r];
+    if (lane == 0) {
+      pp[HD] = mrun;
+      pp[HD + 1] = lrun;
+    }
   }
 }
 
-template <int HD, int GRP>
-__device__ void attn_phase(const MegaArgs &A, int l, int S, int pos, float *tiles) {
-  for (int task = blockIdx.x; task < A.Hkv * S; task += gridDim.x)
-    attn_task<HD, GRP>(A, l, task / S, task % S, S, pos, tiles);
+template <int ACT, int HD, int GRP>
+__device__ void attn_phase(const MegaArgs &A, int l, int S, int p, unsigned char *ring_a, uint32_t *qs) {
+  for (int task = blockIdx.x; task < A.Hkv * S; task += gridDim.x) {
+    __syncthreads();  // a previous task may still read qs
+    attn_task<ACT, HD, GRP>(A, l, task, S, p, ring_a, task == (int)blockIdx.x, qs);
+  }
+  cp_wait<0>();
 }
 
 // Merge the S split states of every query head into o (16-bit rounded).
@@ -197,11 +265,11 @@ __device__ void combine_phase(const MegaArgs &A, int S) {
       const float w = ms == -INFINITY ? 0.f : expf(ms - M);
       Ls = fmaf(w, __ldcg(base + s * (HD + 2) + HD + 1), Ls);
 #pragma unroll
-      for (int r = 0; r < PER; ++r) acc[r] = fmaf(w, __ldcg(base + s * (HD + 2) + lane + 32 * r), acc[r]);
+      for (int r = 0; r < PER; ++r) acc[r] = fmaf(w, __ldcg(base + s * (HD + 2) + lane * PER + r), acc[r]);
     }
     const float inv = 1.0f / Ls;
 #pragma unroll
-    for (int r = 0; r < PER; ++r) A.o[(size_t)h * HD + lane + 32 * r] = round_act(acc[r] * inv, A.act);
+    for (int r = 0; r < PER; ++r) A.o[(size_t)h * HD + lane * PER + r] = round_act(acc[r] * inv, A.act);
   }
 }
 
@@ -212,8 +280,7 @@ __global__ void __launch_bounds__(MW * 32, 1) k_decode_mega(MegaArgs A) {
   float *scratch = smem + A.xs_floats;   // 256 floats
   const int tid = threadIdx.x, warp = tid >> 5, bid = blockIdx.x, nb = gridDim.x;
   char *ring = reinterpret_cast<char *>(scratch + 256) + (size_t)warp * NST * STAGE;
-  unsigned epoch = 0;
-  if (tid == 0) epoch = *(volatile unsigned *)&A.bar[1];
+  unsigned epoch = 0;  // barriers passed (thread 0); the host zeroes the counter before each step
   const int L = A.L;
   const int pos = A.st.len[0];
 
@@ -248,14 +315,49 @@ __global__ void __launch_bounds__(MW * 32, 1) k_decode_mega(MegaArgs A) {
   if (!grid_barrier(A.bar, epoch, A.st.err)) { cp_wait<0>(); return; }
 
   const int S = A.splits;
+  unsigned char *ring_a = reinterpret_cast<unsigned char *>(xs);
+  float *bsum = scratch + 128;
   for (int l = 0; l < L; ++l) {
+    if (l > 0) {
+      // exit decision of layer l (1-based) from its input h(l-1) and output h(l)
+      const float *hp = A.h[(l - 1) & 1], *hc = A.h[l & 1];
+      float dot = 0.f, n1 = 0.f, n2 = 0.f;
+      for (int i = tid * 4; i < A.d; i += blockDim.x * 4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4 *>(hp + i));
+        const float4 y = __ldcg(reinterpret_cast<const float4 *>(hc + i));
+        dot = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, dot))));
+        n1 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, n1))));
+        n2 = fmaf(y.x, y.x, fmaf(y.y, y.y, fmaf(y.z, y.z, fmaf(y.w, y.w, n2))));
+      }
+      dot = block_sum(dot, bsum);
+      n1 = block_sum(n1, bsum + 32);
+      n2 = block_sum(n2, bsum + 64);
+      const Decision dc = decide(A.st, 0, route, l, L, dot, n1, n2);
+      if (bid == 0 && tid == 0 && A.dbg_s) A.dbg_s[(size_t)(l - 1) * A.Bmax] = dc.s;
+      if (dc.exited) {
+        exit_l = l;
+        route = 1;
+        cp_wait<0>();  // drop the backbone items streamed on the old route
+        is = gemv_begin<MW, EPI_QKV>(a, route, ring, bid, nb);
+      }
+    }
     // QKV -> RoPE -> K/V append
     gemv_run<MW, ACT, PRO_NORM, EPI_QKV>(a, route, xs, scratch, ring, is, bid, nb);
-    // the O projection's weights do not depend on attention: start them now
+    // the first K/V tile of this block's attention task (positions < p are
+    // final) and the O projection's weights do not wait for the barrier
+    __syncthreads();  // the activation region is free again
+    {
+      const int task = bid;
+      if (task < A.Hkv * S) {
+        int tb, te;
+        split_tiles(pos, S, task % S, tb, te);
+        attn_issue<HD>(A, l, task / S, tb, te, pos, 0, ring_a);
+      }
+    }
     a = phase_args(A, l, 1);
     is = gemv_begin<MW, EPI_RESID>(a, route, ring, bid, nb);
     if (!grid_barrier(A.bar, epoch, A.st.err)) { cp_wait<0>(); return; }
-    attn_phase<HD, GRP>(A, l, S, pos, xs);
+    attn_phase<ACT, HD, GRP>(A, l, S, pos, ring_a, reinterpret_cast<uint32_t *>(scratch));
     if (!grid_barrier(A.bar, epoch, A.st.err)) { cp_wait<0>(); return; }
     combine_phase<HD>(A, S);
     if (!grid_barrier(A.bar, epoch, A.st.err)) { cp_wait<0>(); return; }
@@ -269,61 +371,34 @@ __global__ void __launch_bounds__(MW * 32, 1) k_decode_mega(MegaArgs A) {
     a = phase_args(A, l, 3);
     is = gemv_begin<MW, EPI_DOWN>(a, route, ring, bid, nb);
     if (!grid_barrier(A.bar, epoch, A.st.err)) { cp_wait<0>(); return; }
-    // down + residual, per-block s(l) sums
-    {
-      PhaseOut po = gemv_run<MW, ACT, PRO_VEC, EPI_DOWN>(a, route, xs, scratch, ring, is, bid, nb);
-      float *bsum = scratch + 128;
-      const float p0 = block_sum(po.p_dot, bsum), p1 = block_sum(po.p_n1, bsum + 32), p2 = block_sum(po.p_n2, bsum + 64);
-      if (tid == 0) {
-        A.partials[bid * 3 + 0] = p0;
-        A.partials[bid * 3 + 1] = p1;
-        A.partials[bid * 3 + 2] = p2;
-      }
-    }
-    if (!grid_barrier(A.bar, epoch, A.st.err)) return;
-    // every block derives the same decision from the same sums in the same order
-    {
-      __shared__ float dsum[3];
-      if (warp == 0) {
-        float t0 = 0.f, t1 = 0.f, t2 = 0.f;
-        for (int i = (tid & 31); i < nb; i += 32) {
-          t0 += __ldcg(A.partials + i * 3 + 0);
-          t1 += __ldcg(A.partials + i * 3 + 1);
-          t2 += __ldcg(A.partials + i * 3 + 2);
-        }
-        t0 = warp_sum(t0);
-        t1 = warp_sum(t1);
-        t2 = warp_sum(t2);
-        if (tid == 0) { dsum[0] = t0; dsum[1] = t1; dsum[2] = t2; }
-      }
-      __syncthreads();
-      const int layer1 = l + 1;
-      const float s = dsum[0] / fmaxf(sqrtf(dsum[1]) * sqrtf(dsum[2]), 1e-8f);
-      float *dbg_s = A.dbg_s ? A.dbg_s + (size_t)l * A.Bmax : nullptr;
-      if (route == 0) {
-        bool go;
-        if (*A.st.mode == 1) {
-          int f = A.st.forced[0];
-          if (f < 0 || f > L) f = L;
-          go = layer1 == f && layer1 < L;
-        } else {
-          go = layer1 >= *A.st.entry && layer1 <= L - 1 && s > *A.st.tau;
-        }
-        if (bid == 0 && tid == 0 && dbg_s) dbg_s[0] = s;
-        if (go) { route = 1; exit_l = layer1; }
-      } else if (bid == 0 && tid == 0 && dbg_s) {
-        dbg_s[0] = __int_as_float(0x7fc00000);
-      }
-      __syncthreads();  // dsum is rewritten next layer
-    }
+    // down + residual
+    gemv_run<MW, ACT, PRO_VEC, EPI_DOWN>(a, route, xs, scratch, ring, is, bid, nb);
     if (l + 1 < L) {
       a = phase_args(A, l + 1, 0);
       is = gemv_begin<MW, EPI_QKV>(a, route, ring, bid, nb);
     }
+    if (!grid_barrier(A.bar, epoch, A.st.err)) { cp_wait<0>(); return; }
+  }
+
+  // s(L) for the debug dump (no exit after the last layer)
+  if (A.dbg_s && bid == 0) {
+    const float *hp = A.h[(L - 1) & 1], *hc = A.h[L & 1];
+    float dot = 0.f, n1 = 0.f, n2 = 0.f;
+    for (int i = tid; i < A.d; i += blockDim.x) {
+      const float x = __ldcg(hp + i), y = __ldcg(hc + i);
+      dot = fmaf(x, y, dot);
+      n1 = fmaf(x, x, n1);
+      n2 = fmaf(y, y, n2);
+    }
+    dot = block_sum(dot, bsum);
+    n1 = block_sum(n1, bsum + 32);
+    n2 = block_sum(n2, bsum + 64);
+    const Decision dc = decide(A.st, 0, route, L, L, dot, n1, n2);
+    if (tid == 0) A.dbg_s[(size_t)(L - 1) * A.Bmax] = dc.s;
   }
 
   // ---- final norm + LM head + greedy pick
-  float *head_part = A.partials + 3 * nb;
+  float *head_part = A.partials;
   a = head_args(A);
   is = gemv_begin<MW, EPI_LOGITS>(a, 0, ring, bid, nb);
   {
@@ -339,8 +414,6 @@ __global__ void __launch_bounds__(MW * 32, 1) k_decode_mega(MegaArgs A) {
       int ib = bi[0];
       for (int q = 1; q < MW * 32; ++q)
         if (bv[q] > vb || (bv[q] == vb && bi[q] < ib)) { vb = bv[q]; ib = bi[q]; }
-      // the head's results go after the s(l) sums: a slow block may still be
-      // reading those for the last decision
       head_part[bid * 2] = vb;
       reinterpret_cast<int *>(head_part)[bid * 2 + 1] = ib;
     }
@@ -421,7 +494,9 @@ cudaError_t mega_launch(const MegaArgs &A, int grid, cudaStream_t s) {
 #undef RV_L
 }
 
-size_t mega_attn_tile_floats(int hd, int grp) { return (size_t)grp * hd + (size_t)ATILE * (hd + 1) + (size_t)ATILE * hd; }
+size_t mega_attn_tile_floats(int hd, int) {
+  return (size_t)2 * ATILE * ((hd * 2 + 16) + hd * 2) / sizeof(float);  // the 2-slot K/V ring
+}
 int mega_warps() { return MW; }
 
 }  // namespace rv
