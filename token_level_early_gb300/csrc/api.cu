@@ -108,6 +108,8 @@ struct rv_model {
   float *gH = nullptr, *gHin = nullptr, *gX = nullptr, *gY = nullptr, *gY2 = nullptr, *gQ = nullptr, *gO = nullptr;
   int32_t *gLists = nullptr, *gTokens = nullptr;
   float *gHf = nullptr, *gXf = nullptr, *gLogits = nullptr;
+  uint16_t *gXb = nullptr;  // 16-bit staging of GEMM rows for the tensor-core path
+  bool tc_gemm = false;     // tcgen05 rows GEMM usable on this device
 
   // debug copies
   bool debug = false;
@@ -288,6 +290,15 @@ int enqueue_step_b1(rv_model *m, cudaStream_t s) {
 
 // -------------------------------------------------------------- general path
 
+// Rows GEMM: the tensor-core kernel for 16-bit matrices where the device has
+// it, the CUDA-core kernel for the int4 river copies.
+static cudaError_t gemm_rows(rv_model *m, const Mat &mt, int river, const float *X, float *Y, const int32_t *list,
+                             const int32_t *count, int max_rows, cudaStream_t s) {
+  if (!river && m->tc_gemm && mt.K % 8 == 0 && max_rows <= m->ws_rows)
+    return launch_gemm_tc(mt, m->act, X, Y, list, count, max_rows, m->gXb, m->st.err, s);
+  return launch_gemm_rows(mt, river, m->act, X, Y, list, count, max_rows, s);
+}
+
 int ensure_ws(rv_model *m, long rows) {
   if (rows <= m->ws_rows) return RV_OK;
   // captured graphs hold workspace pointers: drop them before reallocating
@@ -305,6 +316,7 @@ int ensure_ws(rv_model *m, long rows) {
   RV_ALLOC(L, m->gH, sizeof(float) * rows * d);
   RV_ALLOC(L, m->gHin, sizeof(float) * rows * d);
   RV_ALLOC(L, m->gX, sizeof(float) * rows * xw);
+  RV_ALLOC(L, m->gXb, sizeof(uint16_t) * rows * (xw > (size_t)m->d ? xw : (size_t)m->d));
   RV_ALLOC(L, m->gY, sizeof(float) * rows * yw);
   RV_ALLOC(L, m->gY2, sizeof(float) * rows * d);
   RV_ALLOC(L, m->gQ, sizeof(float) * rows * qd);
@@ -329,7 +341,7 @@ int enqueue_layer_rows(rv_model *m, int l, int B, int T, const int32_t *base, cu
   // attention sub-block
   RV_CK(launch_rmsnorm_rows(m->gH, ly.attn_norm, d, m->c.rms_eps, act, m->gX, nullptr, m->d_nrows, (int)M, s));
   for (int p = 0; p < npath; ++p)
-    RV_CK(launch_gemm_rows(make_mat(m, ly, MAT_QKV), p, act, m->gX, m->gY, lists[p], cnt[p], (int)M, s));
+    RV_CK(gemm_rows(m, make_mat(m, ly, MAT_QKV), p, m->gX, m->gY, lists[p], cnt[p], (int)M, s));
   RopeRowsArgs ra{};
   ra.kv = m->kv; ra.layer = l; ra.H = m->H; ra.Hkv = m->Hkv; ra.hd = m->hd; ra.act = act;
   ra.Y = m->gY; ra.q = m->gQ; ra.rope_cs = m->rope_cs; ra.list = nullptr; ra.count = m->d_nrows;
@@ -352,15 +364,15 @@ int enqueue_layer_rows(rv_model *m, int l, int B, int T, const int32_t *base, cu
     RV_CK(launch_attn_rows(ar, (int)M, s));
   }
   for (int p = 0; p < npath; ++p)
-    RV_CK(launch_gemm_rows(make_mat(m, ly, MAT_O), p, act, m->gO, m->gY2, lists[p], cnt[p], (int)M, s));
+    RV_CK(gemm_rows(m, make_mat(m, ly, MAT_O), p, m->gO, m->gY2, lists[p], cnt[p], (int)M, s));
   RV_CK(launch_resid_rows(m->gH, m->gY2, d, nullptr, m->d_nrows, (int)M, s));
   // MLP sub-block
   RV_CK(launch_rmsnorm_rows(m->gH, ly.mlp_norm, d, m->c.rms_eps, act, m->gX, nullptr, m->d_nrows, (int)M, s));
   for (int p = 0; p < npath; ++p)
-    RV_CK(launch_gemm_rows(make_mat(m, ly, MAT_GU), p, act, m->gX, m->gY, lists[p], cnt[p], (int)M, s));
+    RV_CK(gemm_rows(m, make_mat(m, ly, MAT_GU), p, m->gX, m->gY, lists[p], cnt[p], (int)M, s));
   RV_CK(launch_swiglu_rows(m->gY, m->F, act, m->gX, nullptr, m->d_nrows, (int)M, s));
   for (int p = 0; p < npath; ++p)
-    RV_CK(launch_gemm_rows(make_mat(m, ly, MAT_D), p, act, m->gX, m->gY2, lists[p], cnt[p], (int)M, s));
+    RV_CK(gemm_rows(m, make_mat(m, ly, MAT_D), p, m->gX, m->gY2, lists[p], cnt[p], (int)M, s));
   RV_CK(launch_resid_rows(m->gH, m->gY2, d, nullptr, m->d_nrows, (int)M, s));
   return RV_OK;
 }
@@ -370,7 +382,7 @@ int enqueue_head_rows(rv_model *m, int B, int bump_len, int set_len, cudaStream_
   RV_CK(launch_rmsnorm_rows(m->gHf, m->final_norm, m->d, m->c.rms_eps, m->act, m->gXf, nullptr, m->d_nrows, B, s));
   Mat lm{};
   lm.w = m->lm_head; lm.N = m->V; lm.K = m->d;
-  RV_CK(launch_gemm_rows(lm, 0, m->act, m->gXf, m->gLogits, nullptr, m->d_nrows, B, s));
+  RV_CK(gemm_rows(m, lm, 0, m->gXf, m->gLogits, nullptr, m->d_nrows, B, s));
   RV_CK(launch_argmax_rows(m->gLogits, m->V, B, m->st, bump_len, set_len, s));
   if (m->debug)
     RV_CK(cudaMemcpyAsync(m->dbg_logits, m->gLogits, sizeof(float) * B * m->V, cudaMemcpyDeviceToDevice, s));
@@ -540,6 +552,7 @@ static int load_impl(rv_model *m, const rv_config *cfg, const void *const *weigh
   m->qd = m->H * m->hd; m->kvd = m->Hkv * m->hd; m->qkv_n = m->qd + 2 * m->kvd;
   RV_CK(cudaGetDevice(&m->dev));
   RV_CK(cudaDeviceGetAttribute(&m->n_sm, cudaDevAttrMultiProcessorCount, m->dev));
+  m->tc_gemm = gemm_tc_available();
   const size_t e2 = 2;
   const int d = m->d, F = m->F, V = m->V;
   auto &A = m->allocs;
@@ -756,10 +769,11 @@ static int validate_step(rv_model *m, int B, const int32_t *forced_host, bool fo
 }
 
 // Device error flags -> status: bit 3 = a persistent-kernel grid barrier
-// gave up waiting; the other bits flag invalid inputs (token, forced exit,
-// quantization).
+// gave up waiting, bit 4 = a tensor-core GEMM wait gave up; the other bits
+// flag invalid inputs (token, forced exit, quantization).
 static int device_status(int32_t err) {
   if (err & 8) return fail(RV_ETIMEOUT, "a grid barrier of the persistent decode kernel timed out (0x%x)", err);
+  if (err & 16) return fail(RV_ETIMEOUT, "a bounded wait of the tensor-core GEMM gave up (0x%x)", err);
   return fail(RV_EINVAL, "device flagged an invalid input (0x%x)", err);
 }
 

@@ -117,6 +117,12 @@ cudaError_t launch_route_lists(const int32_t *route, int B, int T, int32_t *list
                                int32_t *counts, cudaStream_t s);
 cudaError_t launch_rmsnorm_rows(const float *H, const uint16_t *gamma, int d, float eps, int act, float *X,
                                 const int32_t *list, const int32_t *count, int max_rows, cudaStream_t s);
+// Tensor-core (tcgen05) rows GEMM for 16-bit matrices: gathers the listed
+// rows of X into xb [max_rows][K] (16-bit) and writes Y[list[r]][n];
+// K % 8 == 0.  Sets bit 16 of *err if a bounded wait gave up.
+bool gemm_tc_available();
+cudaError_t launch_gemm_tc(const Mat &m, int act, const float *X, float *Y, const int32_t *list, const int32_t *count,
+                           int max_rows, uint16_t *xb, int32_t *err, cudaStream_t s);
 cudaError_t launch_gemm_rows(const Mat &m, int river, int act, const float *X, float *Y, const int32_t *list,
                              const int32_t *count, int max_rows, cudaStream_t s);
 struct RopeRowsArgs {
