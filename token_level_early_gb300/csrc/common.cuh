@@ -80,6 +80,28 @@ __device__ __forceinline__ float block_sum(float v, float *scratch) {
   return t;
 }
 
+// Three block sums with one pair of barriers; scratch holds 3 x 32 floats.
+__device__ __forceinline__ float3 block_sum3(float a, float b, float c, float *scratch) {
+  int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  c = warp_sum(c);
+  __syncthreads();
+  if (lane == 0) {
+    scratch[wid] = a;
+    scratch[32 + wid] = b;
+    scratch[64 + wid] = c;
+  }
+  __syncthreads();
+  float3 t = make_float3(0.f, 0.f, 0.f);
+  for (int i = 0; i < nw; ++i) {  // fixed order: deterministic
+    t.x += scratch[i];
+    t.y += scratch[32 + i];
+    t.z += scratch[64 + i];
+  }
+  return t;
+}
+
 // ------------------------------------------------------------------ weights
 
 // River copy of one projection in the device layout: canonical packing with

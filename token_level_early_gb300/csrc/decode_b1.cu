@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
   ItemStream is = gemv_begin<NW, EPI>(a, river, ring, blockIdx.x, gridDim.x);
   pdl_wait();
   pdl_trigger();
+  float ss = -1.f;  // sum of h^2, shared by the decision and the RMSNorm prologue
   if ((EPI == EPI_QKV || EPI == EPI_LOGITS) && a.decide_layer1 > 0) {
     float dot = 0.f, n1 = 0.f, n2 = 0.f;
     for (int i = tid * 4; i < a.m.K; i += blockDim.x * 4) {
@@ -54,9 +55,11 @@ __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
       n1 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, n1))));
       n2 = fmaf(y.x, y.x, fmaf(y.y, y.y, fmaf(y.z, y.z, fmaf(y.w, y.w, n2))));
     }
-    dot = block_sum(dot, bsum);
-    n1 = block_sum(n1, bsum + 32);
-    n2 = block_sum(n2, bsum + 64);
+    const float3 t = block_sum3(dot, n1, n2, bsum);
+    dot = t.x;
+    n1 = t.y;
+    n2 = t.z;
+    ss = n2;
     const int route_now = (EPI == EPI_LOGITS) ? a.st.route[0] : river;
     const Decision dc = decide(a.st, 0, route_now, a.decide_layer1, a.L, dot, n1, n2);
     if (blockIdx.x == 0 && tid == 0) commit_decision(a.st, 0, a.decide_layer1, dc, a.dbg_s);
@@ -66,7 +69,7 @@ __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
       is = gemv_begin<NW, EPI>(a, river, ring, blockIdx.x, gridDim.x);
     }
   }
-  PhaseOut o = gemv_run<NW, ACT, PRO, EPI>(a, river, smem, scratch, ring, is, blockIdx.x, gridDim.x);
+  PhaseOut o = gemv_run<NW, ACT, PRO, EPI>(a, river, smem, scratch, ring, is, blockIdx.x, gridDim.x, ss);
 
   if (EPI == EPI_DOWN) {
     (void)o;  // the next QKV (or the LM head) makes this layer's exit decision

@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(128, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, float *Y, int N, int K,
               const int32_t *list, const int32_t *count, int32_t *err) {
   const int cnt = *count;
-  const int m0 = blockIdx.y * TBM, n0 = blockIdx.x * TBN;
+  // row tiles vary fastest: the CTAs resident at a time share weight tiles in L2
+  const int m0 = blockIdx.x * TBM, n0 = blockIdx.y * TBN;
   if (m0 >= cnt) return;  // no listed row in this tile (before any allocation)
   extern __shared__ uint8_t smraw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -259,7 +260,7 @@ cudaError_t launch_gemm_tc(const Mat &m, int act, const float *X, float *Y, cons
   if (e != cudaSuccess) return e;
   CUtensorMap ta, tb;
   if (!make_map(&ta, xb, max_rows, K, act) || !make_map(&tb, m.w, N, K, act)) return cudaErrorInvalidValue;
-  dim3 grid((N + TBN - 1) / TBN, (max_rows + TBM - 1) / TBM);
+  dim3 grid((max_rows + TBM - 1) / TBM, (N + TBN - 1) / TBN);
   if (grid.y > 65535) return cudaErrorInvalidValue;
   if (act == 1) {
     e = cudaFuncSetAttribute(k_gemm_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TSMEM);

@@ -295,9 +295,10 @@ __device__ __forceinline__ ItemStream gemv_begin(const GemvArgs &a, int river, c
 // (x = round16(RMSNorm(h) * gamma) or x = vec, into the lane layout in xs),
 // the quad loop over the ring, and the epilogue in the owning warp.
 // scratch: 256 floats (cross-warp partials, block sums).
+// ss_in: sum of h^2 when the caller already has it (PRO_NORM), else < 0.
 template <int NWARP, int ACT, int PRO, int EPI>
 __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float *xs, float *scratch, char *ring,
-                                             ItemStream is, int bid, int nblocks) {
+                                             ItemStream is, int bid, int nblocks, float ss_in = -1.f) {
   const PhaseGeo p = phase_geo<NWARP>(a, river);
   const Geo &g = p.g;
   const int nk = p.nk, S = p.S, RG = p.RG, rg = p.rg, sp = p.sp, nquads = p.nquads;
@@ -307,12 +308,15 @@ __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float
 
   float rs = 0.f;
   if (PRO == PRO_NORM) {
-    float ss = 0.f;
-    for (int i = tid * 4; i < g.K; i += blockDim.x * 4) {
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.h + i));
-      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+    float ss = ss_in;
+    if (ss < 0.f) {
+      ss = 0.f;
+      for (int i = tid * 4; i < g.K; i += blockDim.x * 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.h + i));
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+      }
+      ss = block_sum(ss, bsum);
     }
-    ss = block_sum(ss, bsum);
     rs = 1.0f / sqrtf(ss / (float)g.K + a.eps);
   }
   if (river) {

@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(MW * 32, 1) k_decode_mega(MegaArgs A) {
   unsigned char *ring_a = reinterpret_cast<unsigned char *>(xs);
   float *bsum = scratch + 128;
   for (int l = 0; l < L; ++l) {
+    float ss = -1.f;  // sum of h(l)^2, shared by the decision and the RMSNorm prologue
     if (l > 0) {
       // exit decision of layer l (1-based) from its input h(l-1) and output h(l)
       const float *hp = A.h[(l - 1) & 1], *hc = A.h[l & 1];
@@ -329,9 +330,11 @@ __global__ void __launch_bounds__(MW * 32, 1) k_decode_mega(MegaArgs A) {
         n1 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, n1))));
         n2 = fmaf(y.x, y.x, fmaf(y.y, y.y, fmaf(y.z, y.z, fmaf(y.w, y.w, n2))));
       }
-      dot = block_sum(dot, bsum);
-      n1 = block_sum(n1, bsum + 32);
-      n2 = block_sum(n2, bsum + 64);
+      const float3 t = block_sum3(dot, n1, n2, bsum);
+      dot = t.x;
+      n1 = t.y;
+      n2 = t.z;
+      ss = n2;
       const Decision dc = decide(A.st, 0, route, l, L, dot, n1, n2);
       if (bid == 0 && tid == 0 && A.dbg_s) A.dbg_s[(size_t)(l - 1) * A.Bmax] = dc.s;
       if (dc.exited) {
@@ -342,7 +345,7 @@ __global__ void __launch_bounds__(MW * 32, 1) k_decode_mega(MegaArgs A) {
       }
     }
     // QKV -> RoPE -> K/V append
-    gemv_run<MW, ACT, PRO_NORM, EPI_QKV>(a, route, xs, scratch, ring, is, bid, nb);
+    gemv_run<MW, ACT, PRO_NORM, EPI_QKV>(a, route, xs, scratch, ring, is, bid, nb, ss);
     // the first K/V tile of this block's attention task (positions < p are
     // final) and the O projection's weights do not wait for the barrier
     __syncthreads();  // the activation region is free again
