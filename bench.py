@@ -160,7 +160,8 @@ def profile_traffic():
 
 # ------------------------------------------------------------------ our arm
 
-def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=MODES, engine_name="chain"):
+def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=MODES, engine_name="chain",
+                 want_offload=False):
     import torch
     import token_level_early_gb300 as rv
 
@@ -175,7 +176,7 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
     w = synth.make_weights(shape)
     log(f"[{wl_name}] weights generated in {time.time() - t0:.1f}s")
     prompt = synth.make_prompt(shape.vocab, 1, wl.prompt_len)
-    max_seq = wl.prompt_len + (len(MODES) + 1) * (warmup + steps) + steps + 72  # + room for the CPU baseline
+    max_seq = wl.prompt_len + (len(MODES) + 2) * (warmup + steps) + steps + 72  # + room for the CPU baseline
     stream = torch.cuda.Stream()
     t0 = time.time()
     m = rv.Model(shape, w, 1, max_seq, stream=stream.cuda_stream)
@@ -186,7 +187,7 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
     first, e_seq = m.prefill(prompt, wl.prefill_tau)
     log(f"[{wl_name}] prefill {wl.prompt_len} tokens in {time.time() - t0:.1f}s, exit layer {int(e_seq[0])}")
 
-    n_ids = (len(MODES) + 1) * (warmup + steps) + 1
+    n_ids = (len(MODES) + 2) * (warmup + steps) + 1
     d_ids = torch.zeros(n_ids, dtype=torch.int32, device="cuda")
     d_exit = torch.zeros_like(d_ids)
     d_forced = torch.from_numpy(np.concatenate([synth.forced_exits(i, 1, L) for i in range(warmup + steps)])).cuda()
@@ -253,9 +254,29 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
         kern[name] = {"ms": ms, "bytes": by, "gbs": by / (ms / 1e3) / 1e9}
 
     cpu = cpu_baseline(m, shape, w, wl, max_seq, tok, tau, log) if (want_cpu and rank0) else None
+
+    # backbone offloading (the pages' parameter-memory comparison): keep the
+    # first backbone layers on the device, cap the exits there, decode on
+    offload = None
+    if want_offload:
+        keep = 3
+        full_bytes = m.param_bytes(0) + m.param_bytes(1)
+        m.offload_backbone(keep)
+        run_mode("tau", warmup)
+        ctx0 = wl.prompt_len + pos[0]
+        ms, exits, _ = run_mode("tau", steps)
+        resident = m.param_bytes(0) + m.param_bytes(1)
+        by = sum(token_bytes(shape, wl.group, e, ctx0 + i) for i, e in enumerate(exits))
+        offload = {"keep_layers": keep, "resident_param_bytes": resident, "resident_param_gib": resident / 2 ** 30,
+                   "full_param_gib": full_bytes / 2 ** 30, "backbone_16bit_gib": m.param_bytes(0) / 2 ** 30,
+                   "river_gib": m.param_bytes(1) / 2 ** 30, "tau_tokens_per_s": steps / (ms / 1e3),
+                   "achieved_gbs": by / (ms / 1e3) / 1e9, "mean_exit_layer": float(np.mean(exits)),
+                   "pages": "14.96 GiB -> 6.73 GiB (backbone offloading)"}
+        log(f"[{wl_name}] offload keep {keep}: {resident / 2 ** 30:.2f} GiB resident, "
+            f"{offload['tau_tokens_per_s']:.1f} tokens/s")
     m.close()
     return {"modes": results, "e2e_tokens_per_s": steps / e2e_s, "kernels": kern, "cpu": cpu,
-            "prefill_exit": int(e_seq[0])}
+            "prefill_exit": int(e_seq[0]), "offload": offload}
 
 
 def cpu_baseline(gm, shape, w, wl, max_seq, tok, tau, log, budget_s=20.0):
@@ -373,7 +394,7 @@ def main():
     rv.lib()
     modes = tuple(x for x in args.modes.split(",") if x in MODES) or MODES
     res = run_workload(args.workload, args.steps, args.warmup, local, not args.no_cpu_baseline, rank0, log, modes,
-                       args.engine)
+                       args.engine, want_offload="tau" in modes)
     tau_r = res["modes"][modes[0]]
     ms = tau_r["ms_per_step"]
     e2e = res["e2e_tokens_per_s"]
@@ -412,7 +433,7 @@ def main():
             "modes": modes,
             "speedup_vs_full_backbone": (tau_r["tokens_per_s"] / res["modes"]["full"]["tokens_per_s"]
                                          if "full" in res["modes"] else None),
-            "roofline": roof, "kernels": res["kernels"], "cpu_baseline": res["cpu"],
+            "roofline": roof, "kernels": res["kernels"], "cpu_baseline": res["cpu"], "offload": res["offload"],
             "e2e": {"value": world * e2e, "unit": "tokens/s", "h2d_bytes_per_step": 4 * 6,
                     "d2h_bytes_per_step": 4 * 4},
             # per step: the scalar-setting kernel, then the captured chain (step init, embedding, five

@@ -202,9 +202,26 @@ int rv_greedy_head_noalloc(const void *d_lm_head, const void *d_final_norm, cons
                            int d_model, int act_dtype, float rms_eps, int32_t *d_next_id, float *d_logits,
                            void *stream);
 
-/* Sizes, for callers that allocate dump buffers. */
+/* Backbone offloading (paperlayer.ai section 4, "Backbone Offloading": with
+ * most tokens leaving the backbone after a few layers, only the first
+ * backbone layers need to stay on the device next to the river).  Frees the
+ * 16-bit matrices of backbone layers keep_layers+1..L on the device (their
+ * RMSNorm gains stay: the river shares them) and caps every exit at
+ * keep_layers: a row still in the backbone after layer keep_layers
+ * continues in the river, in decode and in prefill.  Needs the river
+ * (RV_ESTATE otherwise); keep_layers in 1..L (RV_EINVAL), not above an
+ * earlier call's value (RV_ESTATE: freed layers cannot come back without
+ * reloading the model); keep_layers = L changes nothing.  Afterwards forced
+ * and fixed exits above keep_layers are RV_EINVAL and rv_param_bytes(m, 0)
+ * counts only the resident backbone. */
+int rv_offload_backbone(rv_model *m, int keep_layers);
+
+/* Sizes, for callers that allocate dump buffers.  rv_param_bytes: which = 0,
+ * the 16-bit parameters resident on the device (embedding, LM head, norms,
+ * backbone layers 1..keep_layers); which = 1, the river (codes and
+ * (scale, zero) words). */
 size_t rv_kv_bytes(const rv_model *m);
-size_t rv_param_bytes(const rv_model *m, int which /* 0 backbone, 1 river */);
+size_t rv_param_bytes(const rv_model *m, int which);
 
 /* Free everything the model owns. */
 void rv_free_model(rv_model *m);

@@ -54,6 +54,7 @@ def lib():
         "ora_create": ([ctypes.POINTER(OraConfig), vp, i32, ctypes.POINTER(vp)], i32),
         "ora_free": ([vp], None),
         "ora_quantize_river": ([vp, i32, i32], i32),
+        "ora_set_exit_cap": ([vp, i32], i32),
         "ora_export_river": ([vp, i32, i32, vp, vp, vp], i32),
         "ora_prefill": ([vp, vp, i32, i32, dbl, i32, vp, vp, vp, vp, vp, vp, vp, vp], i32),
         "ora_decode_step": ([vp, vp, i32, dbl, vp, vp, vp, vp, vp, vp, vp, vp, vp], i32),
@@ -191,6 +192,10 @@ class Model:
         s = self.shape
         d, qd, kvd = s.d_model, s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim
         return [(qd, d), (kvd, d), (kvd, d), (d, qd), (s.ffn, d), (s.ffn, d), (d, s.ffn)][proj]
+
+    def set_exit_cap(self, cap: int) -> int:
+        """Backbone offloading: keep backbone layers 1..cap; exits are capped at cap."""
+        return int(lib().ora_set_exit_cap(self._h, int(cap)))
 
     def quantize_river(self, group: int, entry_layer: int = 1) -> int:
         rc = lib().ora_quantize_river(self._h, group, entry_layer)

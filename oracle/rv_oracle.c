@@ -56,6 +56,7 @@ struct ora_model {
   const uint16_t *embed, *final_norm, *lm_head;
   ora_layer *layers;
   int group, entry, has_river;
+  int cap;      /* last backbone layer kept (L = all): exits are capped there */
   uint16_t *kv; /* [L][2][max_batch][Hkv][max_seq][hd] */
   int32_t *len; /* [max_batch] */
 };
@@ -543,6 +544,16 @@ static int lm_head_pick(ora_model *m, const double *h, double *logits, int tf_id
 /* Prefill: sequence-level exit                                        */
 /* ------------------------------------------------------------------ */
 
+/* Backbone offloading (paperlayer.ai section 4, Backbone Offloading): only
+ * backbone layers 1..cap stay; a row still in the backbone after layer cap
+ * continues in the river.  cap in 1..L; needs the river. */
+int ora_set_exit_cap(ora_model *m, int cap) {
+  if (!m || cap < 1 || cap > m->c.n_layers) return RV_EINVAL;
+  if (!m->has_river && cap < m->c.n_layers) return RV_ESTATE;
+  m->cap = cap;
+  return RV_OK;
+}
+
 int ora_prefill(ora_model *m, const int32_t *tokens, int B, int T0, double tau, int fixed_exit,
                 const int32_t *tf_exit, const int32_t *tf_ids, int32_t *next_ids, int32_t *exit_layer,
                 double *dbg_smin, double *dbg_hidden_last, double *dbg_logits, int32_t *n_forced) {
@@ -550,6 +561,7 @@ int ora_prefill(ora_model *m, const int32_t *tokens, int B, int T0, double tau, 
   const ora_config *c = &m->c;
   int L = c->n_layers, d = c->d_model;
   if (fixed_exit > L || fixed_exit < -1) return RV_EINVAL;
+  if (fixed_exit > m->cap) return RV_EINVAL;
   if (!m->has_river && fixed_exit != L) return RV_ESTATE;
   for (int i = 0; i < B * T0; ++i)
     if (tokens[i] < 0 || tokens[i] >= c->vocab) return RV_EINVAL;
@@ -577,24 +589,25 @@ int ora_prefill(ora_model *m, const int32_t *tokens, int B, int T0, double tau, 
       if (river) continue;
       if (fixed_exit >= 0) {
         if (l == fixed_exit) river = 1;
-        continue;
+      } else if (l >= m->entry && l <= L - 1) {
+        /* the latest-exiting token sets the depth: exit when every token's
+         * similarity exceeds tau, i.e. when the minimum does */
+        double smin = INFINITY;
+        for (int t = 0; t < T0; ++t) {
+          double s = ora_cosine(Hin + (size_t)t * d, Hs + (size_t)t * d, d);
+          if (s < smin) smin = s;
+        }
+        if (dbg_smin) dbg_smin[(size_t)(l - 1) * B + b] = smin;
+        int go = smin > tau;
+        if (tf_exit && fabs(smin - tau) <= TIE_S) {
+          int g2 = tf_exit[b] == l;
+          if (g2 != go && n_forced) n_forced[0]++;
+          go = g2;
+        }
+        if (go) { e_seq = l; river = 1; }
       }
-      if (l < m->entry || l > L - 1) continue;
-      /* the latest-exiting token sets the depth: exit when every token's
-       * similarity exceeds tau, i.e. when the minimum does */
-      double smin = INFINITY;
-      for (int t = 0; t < T0; ++t) {
-        double s = ora_cosine(Hin + (size_t)t * d, Hs + (size_t)t * d, d);
-        if (s < smin) smin = s;
-      }
-      if (dbg_smin) dbg_smin[(size_t)(l - 1) * B + b] = smin;
-      int go = smin > tau;
-      if (tf_exit && fabs(smin - tau) <= TIE_S) {
-        int g2 = tf_exit[b] == l;
-        if (g2 != go && n_forced) n_forced[0]++;
-        go = g2;
-      }
-      if (go) { e_seq = l; river = 1; }
+      /* backbone offloading: layers after the cap exist only in the river */
+      if (!river && l >= m->cap && l < L) { e_seq = l; river = 1; }
     }
     m->len[b] = T0;
     int forced = 0;
@@ -619,7 +632,7 @@ int ora_decode_step(ora_model *m, const int32_t *tokens, int B, double tau, cons
   int L = c->n_layers, d = c->d_model;
   for (int b = 0; b < B; ++b) {
     if (tokens[b] < 0 || tokens[b] >= c->vocab) return RV_EINVAL;
-    if (forced && (forced[b] < 0 || forced[b] > L)) return RV_EINVAL;
+    if (forced && (forced[b] < 0 || forced[b] > L || forced[b] > m->cap)) return RV_EINVAL;
     if (forced && forced[b] < L && !m->has_river) return RV_ESTATE;
   }
   if (!forced && !m->has_river) return RV_ESTATE;
@@ -663,16 +676,17 @@ int ora_decode_step(ora_model *m, const int32_t *tokens, int B, double tau, cons
       if (dbg_s) dbg_s[(size_t)(l - 1) * B + b] = s;
       if (forced) {
         if (l == forced[b] && l < L) { river[b] = 1; exit_layer[b] = l; }
-        continue;
+      } else if (l >= m->entry && l <= L - 1) {
+        int go = s > tau;
+        if (tf_exit && fabs(s - tau) <= TIE_S) {
+          int g2 = tf_exit[b] == l;
+          if (g2 != go && n_forced) n_forced[0]++;
+          go = g2;
+        }
+        if (go) { river[b] = 1; exit_layer[b] = l; }
       }
-      if (l < m->entry || l > L - 1) continue;
-      int go = s > tau;
-      if (tf_exit && fabs(s - tau) <= TIE_S) {
-        int g2 = tf_exit[b] == l;
-        if (g2 != go && n_forced) n_forced[0]++;
-        go = g2;
-      }
-      if (go) { river[b] = 1; exit_layer[b] = l; }
+      /* backbone offloading: layers after the cap exist only in the river */
+      if (!river[b] && l >= m->cap && l < L) { river[b] = 1; exit_layer[b] = l; }
     }
   }
   for (int b = 0; b < B; ++b) {
@@ -745,6 +759,7 @@ int ora_create(const ora_config *cfg, const uint16_t *const *weights, int nthrea
   m->final_norm = weights[1];
   m->lm_head = c->tied_embed ? weights[0] : weights[2];
   m->entry = 1;
+  m->cap = c->n_layers;
   m->layers = (ora_layer *)calloc((size_t)c->n_layers, sizeof(ora_layer));
   for (int l = 0; l < c->n_layers; ++l) {
     const uint16_t *const *w = weights + 3 + 9 * l;

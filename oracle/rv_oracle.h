@@ -41,6 +41,8 @@ void ora_free(ora_model *m);
 int ora_quantize_river(ora_model *m, int group, int entry_layer);
 int ora_export_river(const ora_model *m, int layer, int proj, uint32_t *q, uint16_t *s, uint16_t *z);
 
+/* Backbone offloading: keep backbone layers 1..cap; exits are capped at cap. */
+int ora_set_exit_cap(ora_model *m, int cap);
 int ora_prefill(ora_model *m, const int32_t *tokens, int B, int T0, double tau, int fixed_exit,
                 const int32_t *tf_exit, const int32_t *tf_ids, int32_t *next_ids, int32_t *exit_layer,
                 double *dbg_smin, double *dbg_hidden_last, double *dbg_logits, int32_t *n_forced);

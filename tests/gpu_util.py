@@ -71,20 +71,23 @@ def check_ids(g_next, ol, band):
             f"row {b}: id {g_next[b]} (oracle logit {ol[b][g_next[b]]:.5f}) vs oracle {o_id} ({ol[b][o_id]:.5f})"
 
 
-def check_decisions(s_gpu, g_exit, tau, forced, entry, L):
+def check_decisions(s_gpu, g_exit, tau, forced, entry, L, cap=None):
     """The GPU's exit layer follows its own s(l): first l in [entry, L-1]
-    with s(l) > tau (decisions within the tie band may go either way)."""
+    with s(l) > tau (decisions within the tie band may go either way); with
+    backbone offloading (cap < L) a row still in the backbone exits at cap."""
+    cap = L if cap is None else cap
     for b in range(len(g_exit)):
         e = int(g_exit[b])
+        assert e <= cap, (b, e, cap)
         if forced is not None:
-            assert e == int(forced[b])
+            assert e == min(int(forced[b]), cap)
             continue
         for l in range(1, e + 1):
             s = float(s_gpu[l - 1, b])
             assert np.isfinite(s), (b, l)
             if entry <= l <= L - 1 and l < e:
                 assert s <= tau or abs(s - tau) <= TIE_S, (b, l, s, tau)
-        if e < L:
+        if e < L and e < cap:
             s = float(s_gpu[e - 1, b])
             assert s > tau or abs(s - tau) <= TIE_S, (b, e, s, tau)
         for l in range(e + 1, L + 1):
@@ -92,7 +95,7 @@ def check_decisions(s_gpu, g_exit, tau, forced, entry, L):
 
 
 def check_layerwise(gm, om, kv_pre, lens_pre, g_next, g_exit, B, L, act, tau=None, forced=None, entry=1,
-                    tag=""):
+                    tag="", cap=None):
     """Layer-by-layer comparison from the GPU's own inputs (see module doc)."""
     hid = gm.dump(rv.DUMP_HIDDEN)[:, :B].astype(np.float64)
     s_gpu = gm.dump(rv.DUMP_S)[:, :B]
@@ -128,7 +131,7 @@ def check_layerwise(gm, om, kv_pre, lens_pre, g_next, g_exit, B, L, act, tau=Non
     assert err <= TOL_LOGIT, f"{tag} head logits max-abs {err}"
     check_ids(g_next, ol, TIE_LOGIT)
     if tau is not None or forced is not None:
-        check_decisions(s_gpu, g_exit, tau, forced, entry, L)
+        check_decisions(s_gpu, g_exit, tau, forced, entry, L, cap)
     rec = {"tag": tag, "layer_worst_rel": worst, "kv_worst_rel": kv_worst, "head_logit_err": err}
     log(rec)
     return rec
@@ -150,7 +153,7 @@ def check_free(gm, o, g_next, g_exit, B, L, tag=""):
     return rec
 
 
-def sampled_step(gm, om, toks, tau, forced, B, L, act, entry=1, tag=""):
+def sampled_step(gm, om, toks, tau, forced, B, L, act, entry=1, tag="", cap=None):
     """Run one GPU decode step and check it both ways from the GPU's state."""
     kv_pre = gm.dump(rv.DUMP_KV)
     lens_pre = gm.dump(rv.DUMP_LENS).copy()
@@ -159,5 +162,5 @@ def sampled_step(gm, om, toks, tau, forced, B, L, act, entry=1, tag=""):
     o = om.decode_step(toks, tau, forced=forced, tf_exit=g_exit, tf_ids=g_next, debug=True)
     assert o["rc"] == 0
     check_free(gm, o, g_next, g_exit, B, L, tag)
-    check_layerwise(gm, om, kv_pre, lens_pre, g_next, g_exit, B, L, act, tau, forced, entry, tag)
+    check_layerwise(gm, om, kv_pre, lens_pre, g_next, g_exit, B, L, act, tau, forced, entry, tag, cap)
     return g_next, g_exit

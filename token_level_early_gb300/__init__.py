@@ -28,7 +28,7 @@ PROJ_Q, PROJ_K, PROJ_V, PROJ_O, PROJ_GATE, PROJ_UP, PROJ_DOWN = range(7)
 DUMP_HIDDEN, DUMP_S, DUMP_LOGITS, DUMP_KV, DUMP_LENS = range(5)
 EXPORTED = ("rv_last_error", "rv_load_model", "rv_quantize_river", "rv_export_river", "rv_prefill",
             "rv_decode_step", "rv_decode_step_dev", "rv_sync_status", "rv_kv_reset", "rv_set_debug",
-            "rv_debug_dump", "rv_kv_bytes", "rv_param_bytes", "rv_free_model", "rv_time_kernel", "rv_greedy_head_noalloc",
+            "rv_debug_dump", "rv_kv_bytes", "rv_param_bytes", "rv_free_model", "rv_time_kernel", "rv_greedy_head_noalloc", "rv_offload_backbone",
             "rv_set_option")
 OPT_DECODE_ENGINE, ENGINE_CHAIN, ENGINE_PERSISTENT = 0, 0, 1
 TIME_GATEUP, TIME_O, TIME_LMHEAD = 0, 1, 2
@@ -115,6 +115,7 @@ def lib():
         "rv_debug_dump": ([vp, i32, vp, sz], i32),
         "rv_kv_bytes": ([vp], sz),
         "rv_param_bytes": ([vp, i32], sz),
+        "rv_offload_backbone": ([vp, i32], i32),
         "rv_free_model": ([vp], None),
         "rv_time_kernel": ([vp, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_float),
                             ctypes.POINTER(ctypes.c_double)], i32),
@@ -266,6 +267,10 @@ class Model:
 
     def kv_bytes(self) -> int:
         return int(lib().rv_kv_bytes(self._h))
+
+    def offload_backbone(self, keep_layers: int) -> None:
+        """Free backbone layers keep_layers+1..L on the device; exits are capped at keep_layers."""
+        _check(lib().rv_offload_backbone(self._h, int(keep_layers)))
 
     def param_bytes(self, which: int) -> int:
         return int(lib().rv_param_bytes(self._h, which))

@@ -14,6 +14,7 @@
 
 #include <map>
 #include <string>
+#include <algorithm>
 #include <vector>
 
 #include "../../include/rv.h"
@@ -80,6 +81,7 @@ struct rv_model {
   uint16_t *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
   std::vector<LayerDev> layers;
   int group = 0, entry = 1;
+  int cap = 0;  // last backbone layer on the device (L = all; set by rv_offload_backbone)
   bool has_river = false;
   std::vector<void *> river_allocs;
 
@@ -159,7 +161,7 @@ void drop_graphs(rv_model *m) {
 }
 
 // int32 state block: [in: tokens B | forced B | mode | tau | entry | nrows]
-//                    [out: next B | exit B | err | pad] [route B | len B | counts 2 | pad 2]
+//                    [out: next B | exit B | err | pad] [route B | len B | counts 2 | cap | pad]
 void state_layout(rv_model *m) {
   const int B = m->Bmax;
   m->in_words = 2 * B + 4;
@@ -180,6 +182,7 @@ void state_layout(rv_model *m) {
   st.route = r;
   st.len = r + B;
   m->d_counts = r + 2 * B;
+  st.cap = r + 2 * B + 2;
 }
 
 size_t state_words(int B) { return (size_t)(2 * B + 4) + (2 * B + 2) + (2 * B + 4); }
@@ -341,7 +344,7 @@ int enqueue_layer_rows(rv_model *m, int l, int B, int T, const int32_t *base, cu
   // attention sub-block
   RV_CK(launch_rmsnorm_rows(m->gH, ly.attn_norm, d, m->c.rms_eps, act, m->gX, nullptr, m->d_nrows, (int)M, s));
   for (int p = 0; p < npath; ++p)
-    RV_CK(gemm_rows(m, make_mat(m, ly, MAT_QKV), p, m->gX, m->gY, lists[p], cnt[p], (int)M, s));
+    if (p == 1 || ly.w[MAT_QKV]) RV_CK(gemm_rows(m, make_mat(m, ly, MAT_QKV), p, m->gX, m->gY, lists[p], cnt[p], (int)M, s));
   RopeRowsArgs ra{};
   ra.kv = m->kv; ra.layer = l; ra.H = m->H; ra.Hkv = m->Hkv; ra.hd = m->hd; ra.act = act;
   ra.Y = m->gY; ra.q = m->gQ; ra.rope_cs = m->rope_cs; ra.list = nullptr; ra.count = m->d_nrows;
@@ -364,15 +367,15 @@ int enqueue_layer_rows(rv_model *m, int l, int B, int T, const int32_t *base, cu
     RV_CK(launch_attn_rows(ar, (int)M, s));
   }
   for (int p = 0; p < npath; ++p)
-    RV_CK(gemm_rows(m, make_mat(m, ly, MAT_O), p, m->gO, m->gY2, lists[p], cnt[p], (int)M, s));
+    if (p == 1 || ly.w[MAT_O]) RV_CK(gemm_rows(m, make_mat(m, ly, MAT_O), p, m->gO, m->gY2, lists[p], cnt[p], (int)M, s));
   RV_CK(launch_resid_rows(m->gH, m->gY2, d, nullptr, m->d_nrows, (int)M, s));
   // MLP sub-block
   RV_CK(launch_rmsnorm_rows(m->gH, ly.mlp_norm, d, m->c.rms_eps, act, m->gX, nullptr, m->d_nrows, (int)M, s));
   for (int p = 0; p < npath; ++p)
-    RV_CK(gemm_rows(m, make_mat(m, ly, MAT_GU), p, m->gX, m->gY, lists[p], cnt[p], (int)M, s));
+    if (p == 1 || ly.w[MAT_GU]) RV_CK(gemm_rows(m, make_mat(m, ly, MAT_GU), p, m->gX, m->gY, lists[p], cnt[p], (int)M, s));
   RV_CK(launch_swiglu_rows(m->gY, m->F, act, m->gX, nullptr, m->d_nrows, (int)M, s));
   for (int p = 0; p < npath; ++p)
-    RV_CK(gemm_rows(m, make_mat(m, ly, MAT_D), p, m->gX, m->gY2, lists[p], cnt[p], (int)M, s));
+    if (p == 1 || ly.w[MAT_D]) RV_CK(gemm_rows(m, make_mat(m, ly, MAT_D), p, m->gX, m->gY2, lists[p], cnt[p], (int)M, s));
   RV_CK(launch_resid_rows(m->gH, m->gY2, d, nullptr, m->d_nrows, (int)M, s));
   return RV_OK;
 }
@@ -607,6 +610,12 @@ static int load_impl(rv_model *m, const rv_config *cfg, const void *const *weigh
   RV_CK(cudaMemsetAsync(m->d_state, 0, sizeof(int32_t) * state_words(m->Bmax), m->stream));
   state_layout(m);
   {
+    const int32_t cap = m->L;  // every backbone layer resident
+    m->cap = cap;
+    RV_CK(cudaMemcpyAsync(const_cast<int32_t *>(m->st.cap), &cap, sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
+    RV_CK(cudaStreamSynchronize(m->stream));
+  }
+  {
     cudaError_t e = cudaMallocHost(&m->pinned, sizeof(int32_t) * (m->in_words + m->out_words + 2 * (size_t)m->Bmax));
     if (e != cudaSuccess) {
       m->pinned = nullptr;
@@ -762,6 +771,7 @@ static int validate_step(rv_model *m, int B, const int32_t *forced_host, bool fo
     for (int b = 0; b < B; ++b) {
       if (forced_host[b] < 0 || forced_host[b] > m->L) return fail(RV_EINVAL, "forced exit out of range");
       if (forced_host[b] < m->L && !m->has_river) return fail(RV_ESTATE, "forced exit below L needs the river");
+      if (forced_host[b] > m->cap) return fail(RV_EINVAL, "forced exit %d beyond the resident backbone layers (%d)", forced_host[b], m->cap);
     }
   for (int b = 0; b < B; ++b)
     if (m->h_len[b] >= m->Tmax) return fail(RV_ECAPACITY, "row %d: KV cache full (%d positions)", b, m->Tmax);
@@ -845,6 +855,7 @@ int rv_prefill(rv_model *m, const int32_t *tokens, int B, int T0, float tau, int
   if (B < 1 || B > m->Bmax || T0 < 1 || T0 > m->Tmax) return fail(RV_EINVAL, "B or T0 out of range");
   if (fixed_exit_layer < -1 || fixed_exit_layer > m->L) return fail(RV_EINVAL, "fixed_exit_layer out of range");
   if (!m->has_river && fixed_exit_layer != m->L) return fail(RV_ESTATE, "prefill with exits needs the river");
+  if (fixed_exit_layer > m->cap) return fail(RV_EINVAL, "fixed exit beyond the resident backbone layers (%d)", m->cap);
   if (!(tau == tau)) return fail(RV_EINVAL, "tau is NaN");
   const long M = (long)B * T0;
   if (M > (1L << 24)) return fail(RV_EINVAL, "B x T0 too large");
@@ -976,6 +987,7 @@ int rv_time_kernel(rv_model *m, int kind, int layer, int river, int iters, float
   if (!ms_per_launch || !bytes || iters < 1 || kind < 0 || kind > 2) return fail(RV_EINVAL, "bad argument");
   if (layer < 1 || layer > m->L) return fail(RV_EINVAL, "layer out of range");
   if (river && (!m->has_river || kind == RV_TIME_LMHEAD)) return fail(RV_ESTATE, "no river copy for this kernel");
+  if (!river && kind != RV_TIME_LMHEAD && layer > m->cap) return fail(RV_ESTATE, "backbone layer %d is offloaded", layer);
   cudaStream_t s = m->stream;
   RV_CK(cudaStreamSynchronize(s));
   const int32_t route = river ? 1 : 0;
@@ -1035,13 +1047,38 @@ int rv_time_kernel(rv_model *m, int kind, int layer, int river, int iters, float
 
 size_t rv_kv_bytes(const rv_model *m) { return m ? m->kv_bytes : 0; }
 
+int rv_offload_backbone(rv_model *m, int keep_layers) {
+  g_err.clear();
+  if (check_common(m)) return RV_EINVAL;
+  if (!m->has_river) return fail(RV_ESTATE, "offloading needs the river (rv_quantize_river)");
+  if (keep_layers < 1 || keep_layers > m->L) return fail(RV_EINVAL, "keep_layers must be in 1..L");
+  if (keep_layers > m->cap) return fail(RV_ESTATE, "backbone layers above %d were already offloaded", m->cap);
+  if (keep_layers == m->cap) return RV_OK;
+  RV_CK(cudaStreamSynchronize(m->stream));
+  drop_graphs(m);  // captured steps hold the matrices' pointers
+  for (int l = keep_layers; l < m->L; ++l)
+    for (int i = 0; i < N_MAT; ++i) {
+      void *p = m->layers[l].w[i];
+      if (!p) continue;
+      auto it = std::find(m->allocs.begin(), m->allocs.end(), p);
+      if (it != m->allocs.end()) m->allocs.erase(it);
+      RV_CK(cudaFree(p));
+      m->layers[l].w[i] = nullptr;
+    }
+  const int32_t cap = keep_layers;
+  RV_CK(cudaMemcpy(const_cast<int32_t *>(m->st.cap), &cap, sizeof(int32_t), cudaMemcpyHostToDevice));
+  m->cap = keep_layers;
+  return build_mega(m);
+}
+
 size_t rv_param_bytes(const rv_model *m, int which) {
   if (!m) return 0;
   size_t t = 0;
-  if (which == 0) {
+  if (which == 0) {  // resident 16-bit parameters: embedding, LM head, norms, backbone layers 1..cap
     const size_t d = m->d;
     t = 2 * ((size_t)m->V * d * (m->c.tied_embed ? 1 : 2) + d);
-    t += (size_t)m->L * 2 * (2 * d + (size_t)m->qkv_n * d + d * m->qd + 2 * (size_t)m->F * d + d * m->F);
+    t += (size_t)m->L * 2 * (2 * d);
+    t += (size_t)m->cap * 2 * ((size_t)m->qkv_n * d + d * m->qd + 2 * (size_t)m->F * d + d * m->F);
     return t;
   }
   if (!m->has_river) return 0;

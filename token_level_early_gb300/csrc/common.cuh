@@ -131,6 +131,8 @@ struct StepState {
   const float *tau;       // scalar
   const int32_t *mode;    // scalar: 0 tau rule, 1 forced exits
   const int32_t *entry;   // scalar: first layer eligible for the tau rule
+  const int32_t *cap;     // scalar: last backbone layer kept on the device (L = all); a row still
+                          // in the backbone after layer cap continues in the river
   int32_t *err;           // scalar error flags (bit 0 token, bit 1 forced value, bit 2 quant)
 };
 

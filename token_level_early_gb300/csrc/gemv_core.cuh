@@ -278,6 +278,7 @@ __device__ __forceinline__ PhaseGeo phase_geo(const GemvArgs &a, int river) {
 // may run before the phase's activations exist.
 template <int NWARP, int EPI>
 __device__ __forceinline__ ItemStream gemv_begin(const GemvArgs &a, int river, char *ring, int bid, int nblocks) {
+  if (!a.m.w) river = 1;  // an offloaded backbone layer exists only in the river
   const PhaseGeo p = phase_geo<NWARP>(a, river);
   const int lane = threadIdx.x & 31;
   ItemStream is;
@@ -299,6 +300,7 @@ __device__ __forceinline__ ItemStream gemv_begin(const GemvArgs &a, int river, c
 template <int NWARP, int ACT, int PRO, int EPI>
 __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float *xs, float *scratch, char *ring,
                                              ItemStream is, int bid, int nblocks, float ss_in = -1.f) {
+  if (!a.m.w) river = 1;  // an offloaded backbone layer exists only in the river
   const PhaseGeo p = phase_geo<NWARP>(a, river);
   const Geo &g = p.g;
   const int nk = p.nk, S = p.S, RG = p.RG, rg = p.rg, sp = p.sp, nquads = p.nquads;

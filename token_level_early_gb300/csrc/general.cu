@@ -240,9 +240,13 @@ __global__ void k_seq_decide(StepState st, const float *Hin, const float *H, int
   for (int w = 1; w < nw; ++w) mn = fminf(mn, wmin[w]);
   mn = fminf(mn, wmin[0]);
   if (dbg_smin) dbg_smin[b] = mn;
-  if (fixed_exit >= 0) {
-    if (layer1 == fixed_exit && layer1 < L) { st.route[b] = 1; st.exit_layer[b] = layer1; }
-  } else if (layer1 >= *st.entry && layer1 <= L - 1 && mn > *st.tau) {
+  bool go;
+  if (fixed_exit >= 0)
+    go = layer1 == fixed_exit && layer1 < L;
+  else
+    go = layer1 >= *st.entry && layer1 <= L - 1 && mn > *st.tau;
+  if (layer1 >= *st.cap && layer1 < L) go = true;  // backbone offloaded past the cap
+  if (go) {
     st.route[b] = 1;
     st.exit_layer[b] = layer1;
   }

@@ -61,6 +61,8 @@ __device__ __forceinline__ Decision decide(const StepState &st, int b, int route
   } else {
     d.exited = layer1 >= *st.entry && layer1 <= L - 1 && d.s > *st.tau;
   }
+  // backbone offloading: the layers after the cap exist only in the river
+  if (layer1 >= *st.cap && layer1 < L) d.exited = true;
   if (d.exited) d.route = 1;
   return d;
 }
