@@ -111,6 +111,7 @@ struct rv_model {
   int32_t *gLists = nullptr, *gTokens = nullptr;
   float *gHf = nullptr, *gXf = nullptr, *gLogits = nullptr;
   uint16_t *gXb = nullptr;  // 16-bit staging of GEMM rows for the tensor-core path
+  uint16_t *gWhi = nullptr, *gWlo = nullptr;  // a river matrix split into 16-bit hi + lo (tensor-core rows path)
   bool tc_gemm = false;     // tcgen05 rows GEMM usable on this device
 
   // debug copies
@@ -295,10 +296,18 @@ int enqueue_step_b1(rv_model *m, cudaStream_t s) {
 
 // Rows GEMM: the tensor-core kernel for 16-bit matrices where the device has
 // it, the CUDA-core kernel for the int4 river copies.
+// River rows take the tensor-core path (the matrix split into exact 16-bit
+// hi + lo, two GEMMs) from this many rows up; below it the int4 CUDA-core
+// GEMM reads fewer bytes.
+constexpr long kRiverTcRows = 256;
+
 static cudaError_t gemm_rows(rv_model *m, const Mat &mt, int river, const float *X, float *Y, const int32_t *list,
                              const int32_t *count, int max_rows, cudaStream_t s) {
-  if (!river && m->tc_gemm && mt.K % 8 == 0 && max_rows <= m->ws_rows)
-    return launch_gemm_tc(mt, m->act, X, Y, list, count, max_rows, m->gXb, m->st.err, s);
+  if (m->tc_gemm && mt.K % 8 == 0 && max_rows <= m->ws_rows) {
+    if (!river) return launch_gemm_tc(mt, m->act, X, Y, list, count, max_rows, m->gXb, m->st.err, s);
+    if (max_rows >= kRiverTcRows && m->gWhi)
+      return launch_gemm_tc_river(mt, m->act, X, Y, list, count, max_rows, m->gXb, m->gWhi, m->gWlo, m->st.err, s);
+  }
   return launch_gemm_rows(mt, river, m->act, X, Y, list, count, max_rows, s);
 }
 
@@ -320,6 +329,15 @@ int ensure_ws(rv_model *m, long rows) {
   RV_ALLOC(L, m->gHin, sizeof(float) * rows * d);
   RV_ALLOC(L, m->gX, sizeof(float) * rows * xw);
   RV_ALLOC(L, m->gXb, sizeof(uint16_t) * rows * (xw > (size_t)m->d ? xw : (size_t)m->d));
+  m->gWhi = m->gWlo = nullptr;
+  if (m->tc_gemm && rows >= kRiverTcRows) {
+    size_t wmax = (size_t)m->qkv_n * d;
+    if ((size_t)d * qd > wmax) wmax = (size_t)d * qd;
+    if (2 * F * d > wmax) wmax = 2 * F * d;
+    if ((size_t)d * F > wmax) wmax = (size_t)d * F;
+    RV_ALLOC(L, m->gWhi, sizeof(uint16_t) * wmax);
+    RV_ALLOC(L, m->gWlo, sizeof(uint16_t) * wmax);
+  }
   RV_ALLOC(L, m->gY, sizeof(float) * rows * yw);
   RV_ALLOC(L, m->gY2, sizeof(float) * rows * d);
   RV_ALLOC(L, m->gQ, sizeof(float) * rows * qd);

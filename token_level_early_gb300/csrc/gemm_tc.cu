@@ -112,7 +112,7 @@ __global__ void k_pack_rows(const float *X, int K, int act, const int32_t *list,
 template <int ACT>
 __global__ void __launch_bounds__(128, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, float *Y, int N, int K,
-              const int32_t *list, const int32_t *count, int32_t *err) {
+              const int32_t *list, const int32_t *count, int32_t *err, int accumulate) {
   const int cnt = *count;
   // row tiles vary fastest: the CTAs resident at a time share weight tiles in L2
   const int m0 = blockIdx.x * TBM, n0 = blockIdx.y * TBN;
@@ -195,12 +195,18 @@ __global__ void __launch_bounds__(128, 1)
         float *dst = Y + (size_t)m * N + nb;
         if (nb + 32 <= N && (N & 3) == 0) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4 *>(dst + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                                               __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+          for (int i = 0; i < 32; i += 4) {
+            float4 o = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
+                                   __uint_as_float(v[i + 3]));
+            if (accumulate) {
+              const float4 y = *reinterpret_cast<const float4 *>(dst + i);
+              o.x += y.x; o.y += y.y; o.z += y.z; o.w += y.w;
+            }
+            *reinterpret_cast<float4 *>(dst + i) = o;
+          }
         } else {
           for (int i = 0; i < 32; ++i)
-            if (nb + i < N) dst[i] = __uint_as_float(v[i]);
+            if (nb + i < N) dst[i] = accumulate ? dst[i] + __uint_as_float(v[i]) : __uint_as_float(v[i]);
         }
       }
     }
@@ -208,6 +214,31 @@ __global__ void __launch_bounds__(128, 1)
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tacc), "r"(TBN) : "memory");
+}
+
+// River matrix -> two 16-bit matrices hi + lo with hi = round16(w), lo =
+// round16(w - hi), w = (q - z) * s exact in fp32.  w has at most 16
+// significant bits (a 5-bit integer times an 11-bit fp16 scale), so hi + lo
+// is w exactly for both 16-bit types.
+__global__ void k_river_split(RiverMat r, int N, int K, int act, uint16_t *hi, uint16_t *lo) {
+  const int words = r.Kp >> 3;
+  const long total = (long)N * (K / 8);
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int n = (int)(i / (K / 8)), k0 = (int)(i - (long)n * (K / 8)) * 8;
+    const uint32_t word = r.q[(size_t)n * words + (k0 >> 3)];
+    const float2 sz = __half22float2(r.sz[(size_t)n * r.G + k0 / r.g]);
+    uint16_t h[8], l[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float w = ((float)((word >> (4 * j)) & 0xFu) - sz.y) * sz.x;
+      h[j] = f_to_act(w, act);
+      l[j] = f_to_act(w - act_to_f(h[j], act), act);
+    }
+    *reinterpret_cast<uint4 *>(hi + (size_t)n * K + k0) =
+        make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+    *reinterpret_cast<uint4 *>(lo + (size_t)n * K + k0) =
+        make_uint4(l[0] | (l[1] << 16), l[2] | (l[3] << 16), l[4] | (l[5] << 16), l[6] | (l[7] << 16));
+  }
 }
 
 std::mutex g_mu;
@@ -248,29 +279,61 @@ bool gemm_tc_available() {
   return major >= 10 && encoder() != nullptr;
 }
 
-cudaError_t launch_gemm_tc(const Mat &m, int act, const float *X, float *Y, const int32_t *list, const int32_t *count,
-                           int max_rows, uint16_t *xb, int32_t *err, cudaStream_t s) {
-  if (max_rows <= 0) return cudaSuccess;
-  const int N = m.N, K = m.K;
-  if (K % 8 || !xb || !encoder()) return cudaErrorInvalidValue;
-  const long work = (long)max_rows * (K / 8);
-  const int pg = (int)((work + 255) / 256 < 4096 ? (work + 255) / 256 : 4096);
-  k_pack_rows<<<pg, 256, 0, s>>>(X, K, act, list, count, xb, max_rows);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+namespace {
+
+cudaError_t gemm_tc_run(const void *W, int N, int K, int act, float *Y, const int32_t *list, const int32_t *count,
+                        int max_rows, const uint16_t *xb, int32_t *err, int accumulate, cudaStream_t s) {
   CUtensorMap ta, tb;
-  if (!make_map(&ta, xb, max_rows, K, act) || !make_map(&tb, m.w, N, K, act)) return cudaErrorInvalidValue;
+  if (!make_map(&ta, xb, max_rows, K, act) || !make_map(&tb, W, N, K, act)) return cudaErrorInvalidValue;
   dim3 grid((max_rows + TBM - 1) / TBM, (N + TBN - 1) / TBN);
   if (grid.y > 65535) return cudaErrorInvalidValue;
+  cudaError_t e;
   if (act == 1) {
     e = cudaFuncSetAttribute(k_gemm_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TSMEM);
-    if (e == cudaSuccess) k_gemm_tc<1><<<grid, 128, TSMEM, s>>>(ta, tb, Y, N, K, list, count, err);
+    if (e == cudaSuccess) k_gemm_tc<1><<<grid, 128, TSMEM, s>>>(ta, tb, Y, N, K, list, count, err, accumulate);
   } else {
     e = cudaFuncSetAttribute(k_gemm_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TSMEM);
-    if (e == cudaSuccess) k_gemm_tc<0><<<grid, 128, TSMEM, s>>>(ta, tb, Y, N, K, list, count, err);
+    if (e == cudaSuccess) k_gemm_tc<0><<<grid, 128, TSMEM, s>>>(ta, tb, Y, N, K, list, count, err, accumulate);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+cudaError_t pack_rows(const float *X, int K, int act, const int32_t *list, const int32_t *count, int max_rows,
+                      uint16_t *xb, cudaStream_t s) {
+  const long work = (long)max_rows * (K / 8);
+  const int pg = (int)((work + 255) / 256 < 4096 ? (work + 255) / 256 : 4096);
+  k_pack_rows<<<pg, 256, 0, s>>>(X, K, act, list, count, xb, max_rows);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const Mat &m, int act, const float *X, float *Y, const int32_t *list, const int32_t *count,
+                           int max_rows, uint16_t *xb, int32_t *err, cudaStream_t s) {
+  if (max_rows <= 0) return cudaSuccess;
+  if (m.K % 8 || !xb || !encoder()) return cudaErrorInvalidValue;
+  cudaError_t e = pack_rows(X, m.K, act, list, count, max_rows, xb, s);
+  if (e != cudaSuccess) return e;
+  return gemm_tc_run(m.w, m.N, m.K, act, Y, list, count, max_rows, xb, err, 0, s);
+}
+
+cudaError_t launch_gemm_tc_river(const Mat &m, int act, const float *X, float *Y, const int32_t *list,
+                                 const int32_t *count, int max_rows, uint16_t *xb, uint16_t *whi, uint16_t *wlo,
+                                 int32_t *err, cudaStream_t s) {
+  if (max_rows <= 0) return cudaSuccess;
+  const int N = m.N, K = m.K;
+  if (K % 8 || !xb || !whi || !wlo || !encoder()) return cudaErrorInvalidValue;
+  const long work = (long)N * (K / 8);
+  const int sg = (int)((work + 255) / 256 < 8192 ? (work + 255) / 256 : 8192);
+  k_river_split<<<sg, 256, 0, s>>>(m.r, N, K, act, whi, wlo);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = pack_rows(X, K, act, list, count, max_rows, xb, s);
+  if (e != cudaSuccess) return e;
+  e = gemm_tc_run(whi, N, K, act, Y, list, count, max_rows, xb, err, 0, s);
+  if (e != cudaSuccess) return e;
+  return gemm_tc_run(wlo, N, K, act, Y, list, count, max_rows, xb, err, 1, s);
 }
 
 }  // namespace rv

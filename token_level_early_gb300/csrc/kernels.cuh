@@ -125,6 +125,11 @@ cudaError_t launch_rmsnorm_rows(const float *H, const uint16_t *gamma, int d, fl
 bool gemm_tc_available();
 cudaError_t launch_gemm_tc(const Mat &m, int act, const float *X, float *Y, const int32_t *list, const int32_t *count,
                            int max_rows, uint16_t *xb, int32_t *err, cudaStream_t s);
+// The same for an int4 river matrix: split into 16-bit hi + lo (whi, wlo:
+// [N][K] each, exact), then Y = X hi^T + X lo^T.
+cudaError_t launch_gemm_tc_river(const Mat &m, int act, const float *X, float *Y, const int32_t *list,
+                                 const int32_t *count, int max_rows, uint16_t *xb, uint16_t *whi, uint16_t *wlo,
+                                 int32_t *err, cudaStream_t s);
 cudaError_t launch_gemm_rows(const Mat &m, int river, int act, const float *X, float *Y, const int32_t *list,
                              const int32_t *count, int max_rows, cudaStream_t s);
 struct RopeRowsArgs {
