@@ -321,7 +321,9 @@ def kl_div(a, b):
 def fidelity(wl_name, steps, dev_index, log):
     """River vs full backbone on one token stream (the backbone's greedy ids):
     per step, does the tau-rule model pick the same next token, and
-    KL(backbone || river) of the two next-token distributions."""
+    KL(backbone || river) of the two next-token distributions.  Measured for
+    both river quantizers (RTN and HQQ), with the time each takes to build
+    the river."""
     import torch
     import token_level_early_gb300 as rv
 
@@ -334,30 +336,45 @@ def fidelity(wl_name, steps, dev_index, log):
     prompt = synth.make_prompt(shape.vocab, 1, wl.prompt_len)
     T = wl.prompt_len + steps + 8
     bb = rv.Model(shape, w, 1, T)
-    rl = rv.Model(shape, w, 1, T)
-    rl.quantize_river(wl.group, 1)
-    for m_ in (bb, rl):
+    rivers, build_s = {}, {}
+    for name, method in (("rtn", rv.QUANT_RTN), ("hqq", rv.QUANT_HQQ)):
+        m_ = rv.Model(shape, w, 1, T)
+        m_.set_quantizer(method)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        m_.quantize_river(wl.group, 1)
+        build_s[name] = time.perf_counter() - t0
+        rivers[name] = m_
+    for m_ in (bb, *rivers.values()):
         m_.set_debug(True)
     nb, _ = bb.prefill(prompt, tau, fixed_exit=L)
-    rl.prefill(prompt, wl.prefill_tau)
+    for m_ in rivers.values():
+        m_.prefill(prompt, wl.prefill_tau)
     tok = int(nb[0])
     full = np.array([L], dtype=np.int32)
-    match, kls, exits = 0, [], []
+    match = {k: 0 for k in rivers}
+    kls = {k: [] for k in rivers}
+    exits = {k: [] for k in rivers}
     for _ in range(steps):
         ib, _ = bb.decode_step([tok], tau, full)
         lb = bb.dump(rv.DUMP_LOGITS)[0].copy()
-        ir, er = rl.decode_step([tok], tau)
-        lr = rl.dump(rv.DUMP_LOGITS)[0]
-        match += int(ib[0] == ir[0])
-        kls.append(kl_div(lb, lr))
-        exits.append(int(er[0]))
+        for k, m_ in rivers.items():
+            ir, er = m_.decode_step([tok], tau)
+            match[k] += int(ib[0] == ir[0])
+            kls[k].append(kl_div(lb, m_.dump(rv.DUMP_LOGITS)[0]))
+            exits[k].append(int(er[0]))
         tok = int(ib[0])
     bb.close()
-    rl.close()
-    out = {"workload": wl_name, "tau": tau, "steps": steps, "next_token_match": match / steps,
-           "kl_mean": float(np.mean(kls)), "kl_max": float(np.max(kls)), "mean_exit_layer": float(np.mean(exits)),
+    for m_ in rivers.values():
+        m_.close()
+    out = {"workload": wl_name, "tau": tau, "steps": steps,
            "pages": "98.03% next-token match, KL 0.0045 (trained models)"}
-    log(f"[fidelity] {wl_name}: match {out['next_token_match']:.3f}, KL mean {out['kl_mean']:.4g}")
+    for k in rivers:
+        out[k] = {"next_token_match": match[k] / steps, "kl_mean": float(np.mean(kls[k])),
+                  "kl_max": float(np.max(kls[k])), "mean_exit_layer": float(np.mean(exits[k])),
+                  "river_build_s": build_s[k]}
+        log(f"[fidelity] {wl_name} {k}: match {out[k]['next_token_match']:.3f}, KL mean {out[k]['kl_mean']:.4g}, "
+            f"river built in {build_s[k]:.2f} s")
     return out
 
 

@@ -163,6 +163,16 @@ int rv_debug_dump(rv_model *m, int what, void *dst, size_t bytes);
 #define RV_OPT_DECODE_ENGINE 0
 #define RV_ENGINE_CHAIN 0
 #define RV_ENGINE_PERSISTENT 1
+/* RV_OPT_QUANTIZER selects how the next rv_quantize_river builds the river,
+ * in the same packed format: RV_QUANT_RTN (default, integer fp16 zero) or
+ * RV_QUANT_HQQ (the pages' quantizer, paperlayer.ai appendix A.1: the same
+ * min/max scale, a float zero (stored as fp16) minimising the lp (p = 0.7)
+ * norm of the error by half-quadratic splitting: beta 10, kappa 1.01, at
+ * most 20 iterations, stopping when the mean absolute error stops falling;
+ * deterministic, bit-identical to the oracle). */
+#define RV_OPT_QUANTIZER 1
+#define RV_QUANT_RTN 0
+#define RV_QUANT_HQQ 1
 int rv_set_option(rv_model *m, int option, int value);
 
 /* Kernel timing for roofline reports: launch one batch-1 GEMV kernel of the

@@ -55,6 +55,7 @@ def lib():
         "ora_free": ([vp], None),
         "ora_quantize_river": ([vp, i32, i32], i32),
         "ora_set_exit_cap": ([vp, i32], i32),
+        "ora_set_quantizer": ([vp, i32], i32),
         "ora_export_river": ([vp, i32, i32, vp, vp, vp], i32),
         "ora_prefill": ([vp, vp, i32, i32, dbl, i32, vp, vp, vp, vp, vp, vp, vp, vp], i32),
         "ora_decode_step": ([vp, vp, i32, dbl, vp, vp, vp, vp, vp, vp, vp, vp, vp], i32),
@@ -74,6 +75,8 @@ def lib():
         "ora_attention": ([vp, vp, vp, i32, i32, i32, vp], None),
         "ora_argmax": ([vp, i32], i32),
         "ora_rtn_group": ([vp, i32, i32, vp, vp, vp], i32),
+        "ora_hqq_group": ([vp, i32, i32, vp, vp, vp], i32),
+        "ora_hqq_pow_pm1": ([ctypes.c_float], ctypes.c_float),
         "ora_silu": ([dbl], dbl),
     }
     for name, (args, res) in sig.items():
@@ -150,6 +153,20 @@ def rtn_group(w_bits, act: int):
     return q, s.value, z.value, rc
 
 
+def hqq_pow_pm1(a: float) -> float:
+    return float(lib().ora_hqq_pow_pm1(ctypes.c_float(a)))
+
+
+def hqq_group(w_bits, act: int):
+    """HQQ for one group: returns (q uint8[n], s fp16 bits, z fp16 bits, rc)."""
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    q = np.zeros(w.size, dtype=np.uint8)
+    s = ctypes.c_uint16(0)
+    z = ctypes.c_uint16(0)
+    rc = lib().ora_hqq_group(_p(w), w.size, act, _p(q), ctypes.addressof(s), ctypes.addressof(z))
+    return q, s.value, z.value, rc
+
+
 # ---------------------------------------------------------------- model
 
 def _cfg(shape, max_batch: int, max_seq: int) -> OraConfig:
@@ -192,6 +209,10 @@ class Model:
         s = self.shape
         d, qd, kvd = s.d_model, s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim
         return [(qd, d), (kvd, d), (kvd, d), (d, qd), (s.ffn, d), (s.ffn, d), (d, s.ffn)][proj]
+
+    def set_quantizer(self, method: int) -> int:
+        """River quantizer for the next quantize_river: 0 RTN, 1 HQQ."""
+        return int(lib().ora_set_quantizer(self._h, int(method)))
 
     def set_exit_cap(self, cap: int) -> int:
         """Backbone offloading: keep backbone layers 1..cap; exits are capped at cap."""

@@ -57,6 +57,7 @@ struct ora_model {
   ora_layer *layers;
   int group, entry, has_river;
   int cap;      /* last backbone layer kept (L = all): exits are capped there */
+  int quantizer; /* river quantizer: 0 RTN, 1 HQQ */
   uint16_t *kv; /* [L][2][max_batch][Hkv][max_seq][hd] */
   int32_t *len; /* [max_batch] */
 };
@@ -282,6 +283,115 @@ int ora_rtn_group(const uint16_t *w, int n, int act, uint8_t *q, uint16_t *s_out
   return RV_OK;
 }
 
+/* HQQ (Badri and Shaji, "Half-Quadratic Quantization of Large Machine
+ * Learning Models", 2023; the pages' river quantizer, paperlayer.ai appendix
+ * A.1): the scale stays the min/max one, s = fp16_rn((mx - mn) / 15), and the
+ * float zero z (start: -mn / s) minimises the lp norm (p = 0.7) of the
+ * dequantization error by half-quadratic splitting.  Per iteration, in this
+ * order: q = clamp(rint(w / s + z), 0, 15); w_r = (q - z) s;
+ * e = shrink(w - w_r, beta) with shrink(x) = sign(x) max(|x| - |x|^(p-1) / beta, 0);
+ * z = mean(q - (w - e) / s); beta = beta * kappa; the mean |w - w_r| must keep
+ * falling, else stop (the zero of the stopping iteration is kept).  beta = 10,
+ * kappa = 1.01, at most 20 iterations.  Reading of the pages' storage: the
+ * final zero is rounded to fp16 and the codes are taken again with it, so
+ * (q - z) s is the stored dequantization.  Degenerate groups as in RTN.
+ * Every step is one IEEE fp32 operation; |x|^(p-1) = 2^((p-1) log2 x) with
+ * log2 from the atanh series on the mantissa, log2(m) = (2 / ln 2)(u + u^3/3
+ * + ... + u^11/11), u = (m - 1)/(m + 1), and 2^f = e^(f ln 2) from its Taylor
+ * series to degree 8, so the GPU quantizer can repeat it bit for bit. */
+static float hqq_pow_pm1(float a) { /* a^(p - 1), p = 0.7, a > 0 finite */
+  uint32_t b;
+  memcpy(&b, &a, 4);
+  int ex = (int)(b >> 23);
+  if (ex == 0) { /* subnormal: scale by 2^64 */
+    float t = a * 18446744073709551616.0f;
+    memcpy(&b, &t, 4);
+    ex = (int)(b >> 23) - 64;
+  }
+  ex -= 127;
+  const uint32_t mb = (b & 0x7FFFFFu) | 0x3F800000u;
+  float m;
+  memcpy(&m, &mb, 4);
+  const float u = (m - 1.0f) / (m + 1.0f), u2 = u * u;
+  float ser = 1.0f / 11.0f;
+  ser = ser * u2 + 1.0f / 9.0f;
+  ser = ser * u2 + 1.0f / 7.0f;
+  ser = ser * u2 + 1.0f / 5.0f;
+  ser = ser * u2 + 1.0f / 3.0f;
+  ser = ser * u2 + 1.0f;
+  const float lg = (float)ex + (ser * u) * 2.88539008f;
+  const float y = -0.3f * lg;
+  const float fi = floorf(y), f = y - fi;
+  const float t = f * 0.693147182f;
+  float ep = 1.0f / 40320.0f;
+  ep = ep * t + 1.0f / 5040.0f;
+  ep = ep * t + 1.0f / 720.0f;
+  ep = ep * t + 1.0f / 120.0f;
+  ep = ep * t + 1.0f / 24.0f;
+  ep = ep * t + 1.0f / 6.0f;
+  ep = ep * t + 0.5f;
+  ep = ep * t + 1.0f;
+  ep = ep * t + 1.0f;
+  const int i = (int)fi;
+  const uint32_t pb = (uint32_t)(i + 127) << 23;
+  float p2;
+  memcpy(&p2, &pb, 4);
+  return ep * p2;
+}
+
+/* The |x|^(p-1) step alone, for its pin against the mathematical power. */
+float ora_hqq_pow_pm1(float a) { return hqq_pow_pm1(a); }
+
+int ora_hqq_group(const uint16_t *w, int n, int act, uint8_t *q, uint16_t *s_out, uint16_t *z_out) {
+  float mn = INFINITY, mx = -INFINITY;
+  for (int i = 0; i < n; ++i) {
+    float v = (float)ora_act16_decode(w[i], act);
+    if (v < mn) mn = v;
+    if (v > mx) mx = v;
+  }
+  float range = mx - mn;
+  float sf = range / 15.0f;
+  uint16_t s16 = ora_act16_encode((double)sf, 0);
+  float s = f16_bits_to_float(s16);
+  if (isinf(s) || isnan(s)) return RV_EINVAL;
+  if (s == 0.0f) return ora_rtn_group(w, n, act, q, s_out, z_out); /* degenerate: s = 1, z = 0 */
+  float z = -mn / s, beta = 10.0f, best = INFINITY;
+  for (int it = 0; it < 20; ++it) {
+    float zsum = 0.0f, esum = 0.0f;
+    for (int i = 0; i < n; ++i) {
+      const float v = (float)ora_act16_decode(w[i], act);
+      float r = rintf(v / s + z);
+      if (r < 0.0f) r = 0.0f;
+      if (r > 15.0f) r = 15.0f;
+      const float wr = (r - z) * s, res = v - wr;
+      float e = 0.0f;
+      if (res != 0.0f) {
+        const float a = fabsf(res), sh = a - hqq_pow_pm1(a) / beta;
+        if (sh > 0.0f) e = res < 0.0f ? -sh : sh;
+      }
+      zsum = zsum + (r - (v - e) / s);
+      esum = esum + fabsf(res);
+    }
+    z = zsum / (float)n;
+    beta = beta * 1.01f;
+    const float err = esum / (float)n;
+    if (err < best) best = err;
+    else break;
+  }
+  const uint16_t z16 = ora_act16_encode((double)z, 0);
+  const float zq = f16_bits_to_float(z16);
+  for (int i = 0; i < n; ++i) {
+    const float v = (float)ora_act16_decode(w[i], act);
+    float r = rintf(v / s + zq);
+    if (r < 0.0f) r = 0.0f;
+    if (r > 15.0f) r = 15.0f;
+    q[i] = (uint8_t)r;
+  }
+  *s_out = s16;
+  *z_out = z16;
+  return RV_OK;
+}
+
 static void proj_dims(const ora_config *c, int proj, int *N, int *K) {
   int d = c->d_model, qd = c->n_heads * c->head_dim, kvd = c->n_kv_heads * c->head_dim;
   switch (proj) {
@@ -304,8 +414,10 @@ static void quant_rows(void *p, int lo, int hi) {
     const uint16_t *row = qc->ly->w[qc->proj] + (size_t)n * K;
     for (int gi = 0; gi < G; ++gi) {
       int k0 = gi * g, cnt = K - k0 < g ? K - k0 : g;
-      if (ora_rtn_group(row + k0, cnt, m->c.act_dtype, qq + k0, &qc->ly->rs[qc->proj][(size_t)n * G + gi],
-                        &qc->ly->rz[qc->proj][(size_t)n * G + gi]) != RV_OK)
+      int (*quant)(const uint16_t *, int, int, uint8_t *, uint16_t *, uint16_t *) =
+          m->quantizer == 1 ? ora_hqq_group : ora_rtn_group;
+      if (quant(row + k0, cnt, m->c.act_dtype, qq + k0, &qc->ly->rs[qc->proj][(size_t)n * G + gi],
+                &qc->ly->rz[qc->proj][(size_t)n * G + gi]) != RV_OK)
         qc->err = 1;
     }
     /* canonical packing: word w of row n holds q[n][8w + j] in bits 4j..4j+3 */
@@ -551,6 +663,13 @@ int ora_set_exit_cap(ora_model *m, int cap) {
   if (!m || cap < 1 || cap > m->c.n_layers) return RV_EINVAL;
   if (!m->has_river && cap < m->c.n_layers) return RV_ESTATE;
   m->cap = cap;
+  return RV_OK;
+}
+
+/* River quantizer for the next ora_quantize_river: 0 RTN, 1 HQQ. */
+int ora_set_quantizer(ora_model *m, int method) {
+  if (!m || (method != 0 && method != 1)) return RV_EINVAL;
+  m->quantizer = method;
   return RV_OK;
 }
 

@@ -41,6 +41,11 @@ void ora_free(ora_model *m);
 int ora_quantize_river(ora_model *m, int group, int entry_layer);
 int ora_export_river(const ora_model *m, int layer, int proj, uint32_t *q, uint16_t *s, uint16_t *z);
 
+/* River quantizer for the next ora_quantize_river: 0 RTN, 1 HQQ. */
+int ora_set_quantizer(ora_model *m, int method);
+/* One group of n 16-bit weights by HQQ: codes, fp16 scale and zero. */
+int ora_hqq_group(const uint16_t *w, int n, int act, uint8_t *q, uint16_t *s_out, uint16_t *z_out);
+float ora_hqq_pow_pm1(float a); /* a^(p - 1), p = 0.7, the HQQ shrink's power */
 /* Backbone offloading: keep backbone layers 1..cap; exits are capped at cap. */
 int ora_set_exit_cap(ora_model *m, int cap);
 int ora_prefill(ora_model *m, const int32_t *tokens, int B, int T0, double tau, int fixed_exit,

@@ -31,6 +31,7 @@ EXPORTED = ("rv_last_error", "rv_load_model", "rv_quantize_river", "rv_export_ri
             "rv_debug_dump", "rv_kv_bytes", "rv_param_bytes", "rv_free_model", "rv_time_kernel", "rv_greedy_head_noalloc", "rv_offload_backbone",
             "rv_set_option")
 OPT_DECODE_ENGINE, ENGINE_CHAIN, ENGINE_PERSISTENT = 0, 0, 1
+OPT_QUANTIZER, QUANT_RTN, QUANT_HQQ = 1, 0, 1
 TIME_GATEUP, TIME_O, TIME_LMHEAD = 0, 1, 2
 
 
@@ -236,6 +237,10 @@ class Model:
 
     def set_engine(self, engine: int):
         self.set_option(OPT_DECODE_ENGINE, engine)
+
+    def set_quantizer(self, method: int):
+        """River quantizer of the next quantize_river: QUANT_RTN or QUANT_HQQ."""
+        self.set_option(OPT_QUANTIZER, method)
 
     def set_debug(self, enable: bool):
         _check(lib().rv_set_debug(self._h, 1 if enable else 0))

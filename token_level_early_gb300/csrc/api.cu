@@ -82,6 +82,7 @@ struct rv_model {
   std::vector<LayerDev> layers;
   int group = 0, entry = 1;
   int cap = 0;  // last backbone layer on the device (L = all; set by rv_offload_backbone)
+  int quantizer = RV_QUANT_RTN;  // river quantizer of the next rv_quantize_river
   bool has_river = false;
   std::vector<void *> river_allocs;
 
@@ -737,7 +738,10 @@ int rv_quantize_river(rv_model *m, int group_size, int entry_layer) {
       auto &A = m->river_allocs;
       RV_ALLOC(A, r.q, sizeof(uint32_t) * (size_t)mt.N * (r.Kp / 8));
       RV_ALLOC(A, r.sz, sizeof(__half2) * (size_t)mt.N * r.G);
-      RV_CK(launch_rtn_quantize(mt.w, mt.N, mt.K, m->act, group_size, r.Kp, r.q, r.sz, m->st.err, m->stream));
+      if (m->quantizer == RV_QUANT_HQQ)
+        RV_CK(launch_hqq_quantize(mt.w, mt.N, mt.K, m->act, group_size, r.Kp, r.q, r.sz, m->st.err, m->stream));
+      else
+        RV_CK(launch_rtn_quantize(mt.w, mt.N, mt.K, m->act, group_size, r.Kp, r.q, r.sz, m->st.err, m->stream));
     }
   }
   int32_t err = 0;
@@ -966,6 +970,11 @@ int rv_set_debug(rv_model *m, int enable) {
 int rv_set_option(rv_model *m, int option, int value) {
   g_err.clear();
   if (check_common(m)) return RV_EINVAL;
+  if (option == RV_OPT_QUANTIZER) {
+    if (value != RV_QUANT_RTN && value != RV_QUANT_HQQ) return fail(RV_EINVAL, "unknown quantizer %d", value);
+    m->quantizer = value;  // used by the next rv_quantize_river
+    return RV_OK;
+  }
   if (option != RV_OPT_DECODE_ENGINE) return fail(RV_EINVAL, "unknown option %d", option);
   if (value != RV_ENGINE_CHAIN && value != RV_ENGINE_PERSISTENT) return fail(RV_EINVAL, "unknown engine %d", value);
   if (value == RV_ENGINE_PERSISTENT && !m->mega_ready)

@@ -157,6 +157,8 @@ cudaError_t launch_copy_rows(const float *src, int src_stride, float *dst, int d
                              cudaStream_t s);
 
 // ---------------------------------------------------------------- river construction
+cudaError_t launch_hqq_quantize(const uint16_t *W, int N, int K, int act, int g, int Kp, uint32_t *q, __half2 *sz,
+                                int32_t *err, cudaStream_t s);
 cudaError_t launch_rtn_quantize(const uint16_t *W, int N, int K, int act, int g, int Kp, uint32_t *q, __half2 *sz,
                                 int32_t *err, cudaStream_t s);
 cudaError_t launch_rope_table(float2 *cs, int T, int hd, double theta, cudaStream_t s);
