@@ -154,19 +154,69 @@ __host__ __device__ __forceinline__ size_t smem_bytes(const Geo &g, int nwarp) {
   return sizeof(float) * (x_floats(g) + 256) + (size_t)nwarp * NST * STAGE;
 }
 
-// Eight consecutive activations x[k0..k0+8) (k0 a multiple of 8, all < K).
+// Activation prologue: x = round16(RMSNorm(h) * gamma) (PRO_NORM, r the
+// reciprocal RMS) or x = vec, staged in shared memory as 16-bit pairs in the
+// layout of the path.  Thread t of a pass handles the 8 activations
+// x[8t..8t+8), so a warp's loads cover 1 KB of contiguous fp32; every thread
+// issues the loads of SB passes before it converts and stores, so the
+// L2 round trips overlap instead of running one after the other.
+//   16-bit path: word t (= chunk c * 32 + lane) holds x[8t..8t+8) as 4 pairs.
+//   int4 path:   chunk c, lane ln, word j of the lane's 32-code run, t =
+//                c * 128 + ln * 4 + j: the pairs (x[8t+p], x[8t+p+4]); and per
+//                lane run the sum X of its 32 activations (4 words, summed by
+//                a 4-lane shuffle).
 template <int ACT, int PRO>
-__device__ __forceinline__ void load_x8(const GemvArgs &a, int k0, float r, float *x) {
-  // activations come from other blocks of the same step: read them at L2
-  const float4 *src = reinterpret_cast<const float4 *>((PRO == PRO_NORM ? a.h : a.vec) + k0);
-  const float4 u0 = __ldcg(src), u1 = __ldcg(src + 1);
-  x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
-  x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
-  if (PRO == PRO_NORM) {
-    const uint4 gw = *reinterpret_cast<const uint4 *>(a.gamma + k0);
-    const uint16_t *gp = reinterpret_cast<const uint16_t *>(&gw);
+__device__ __forceinline__ void stage_x(const GemvArgs &a, const Geo &g, int river, int nk, float r, float *xs) {
+  constexpr int SB = 4;
+  const int nt = river ? nk * 128 : nk * 32;  // a multiple of 32: warps stay converged
+  const float *src = PRO == PRO_NORM ? a.h : a.vec;
+  uint4 *xw = reinterpret_cast<uint4 *>(xs);
+  float *xsum = xs + nk * 4 * 32 * 4;
+  const int nthr = (int)blockDim.x;
+  for (int t0 = (int)threadIdx.x; t0 < nt; t0 += SB * nthr) {
+    float4 u[SB][2];
+    uint4 gw[SB];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = round_act(x[j] * r * act_to_f(gp[j], ACT), ACT);
+    for (int i = 0; i < SB; ++i) {
+      const int t = t0 + i * nthr;
+      u[i][0] = u[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      gw[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (t < nt && t * 8 < g.K) {
+        // activations come from other blocks of the same step: read them at L2
+        const float4 *sp = reinterpret_cast<const float4 *>(src + t * 8);
+        u[i][0] = __ldcg(sp);
+        u[i][1] = __ldcg(sp + 1);
+        if (PRO == PRO_NORM) gw[i] = *reinterpret_cast<const uint4 *>(a.gamma + t * 8);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < SB; ++i) {
+      const int t = t0 + i * nthr;
+      if (t0 + i * nthr - (int)(threadIdx.x & 31) >= nt) break;  // the whole warp is past the end
+      float x[8] = {u[i][0].x, u[i][0].y, u[i][0].z, u[i][0].w, u[i][1].x, u[i][1].y, u[i][1].z, u[i][1].w};
+      if (PRO == PRO_NORM) {
+        const uint16_t *gp = reinterpret_cast<const uint16_t *>(&gw[i]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = round_act(x[j] * r * act_to_f(gp[j], ACT), ACT);
+      }
+      if (river) {
+        uint32_t pr[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          pr[q] = (uint32_t)f_to_act(x[q], ACT) | ((uint32_t)f_to_act(x[q + 4], ACT) << 16);
+        const int c = t >> 7, ln = (t >> 2) & 31, j = t & 3;
+        xw[(c * 4 + j) * 32 + ln] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+        float X = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+        X += __shfl_xor_sync(0xffffffffu, X, 1);
+        X += __shfl_xor_sync(0xffffffffu, X, 2);
+        if (j == 0) xsum[c * 32 + ln] = X;
+      } else {
+        xw[t] = make_uint4((uint32_t)f_to_act(x[0], ACT) | ((uint32_t)f_to_act(x[1], ACT) << 16),
+                           (uint32_t)f_to_act(x[2], ACT) | ((uint32_t)f_to_act(x[3], ACT) << 16),
+                           (uint32_t)f_to_act(x[4], ACT) | ((uint32_t)f_to_act(x[5], ACT) << 16),
+                           (uint32_t)f_to_act(x[6], ACT) | ((uint32_t)f_to_act(x[7], ACT) << 16));
+      }
+    }
   }
 }
 
@@ -321,37 +371,7 @@ __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float
     }
     rs = 1.0f / sqrtf(ss / (float)g.K + a.eps);
   }
-  if (river) {
-    uint4 *xq = reinterpret_cast<uint4 *>(xs);       // [nk][4][32]: word j's pairs (x[8j+p], x[8j+p+4])
-    float *xsum = xs + nk * 4 * 32 * 4;              // [nk][32]: sum of the lane run's 32 activations
-    for (int t = tid; t < nk * 32; t += blockDim.x) {
-      const int c = t >> 5, ln = t & 31, base = c * CH4 + ln * 32;
-      float X = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (base + 8 * j < g.K) load_x8<ACT, PRO>(a, base + 8 * j, rs, x);
-        uint32_t pr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          pr[i] = (uint32_t)f_to_act(x[i], ACT) | ((uint32_t)f_to_act(x[i + 4], ACT) << 16);
-        xq[(c * 4 + j) * 32 + ln] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-        X += ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
-      }
-      xsum[c * 32 + ln] = X;
-    }
-  } else {
-    uint4 *xb = reinterpret_cast<uint4 *>(xs);  // [nk][32]: the lane's 8 activations as 16-bit pairs
-    for (int t = tid; t < nk * 32; t += blockDim.x) {
-      const int c = t >> 5, ln = t & 31, base = c * CH16 + ln * 8;
-      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (base < g.K) load_x8<ACT, PRO>(a, base, rs, x);
-      xb[c * 32 + ln] = make_uint4((uint32_t)f_to_act(x[0], ACT) | ((uint32_t)f_to_act(x[1], ACT) << 16),
-                                   (uint32_t)f_to_act(x[2], ACT) | ((uint32_t)f_to_act(x[3], ACT) << 16),
-                                   (uint32_t)f_to_act(x[4], ACT) | ((uint32_t)f_to_act(x[5], ACT) << 16),
-                                   (uint32_t)f_to_act(x[6], ACT) | ((uint32_t)f_to_act(x[7], ACT) << 16));
-    }
-  }
+  stage_x<ACT, PRO>(a, g, river, nk, rs, xs);
   __syncthreads();
 
   const int pos = (EPI == EPI_QKV) ? a.st.len[0] : 0;
