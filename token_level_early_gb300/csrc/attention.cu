@@ -163,7 +163,8 @@ __global__ void __launch_bounds__(GRP * 32, 1) k_attn_dec(AttnArgs a) {
   using TL = DecTile<HD>;
   constexpr int NT = GRP * 32, PER = HD / 32, PR = HD / 8;
   extern __shared__ __align__(16) unsigned char sm[];
-  float *part = reinterpret_cast<float *>(sm + DNST * TL::BYTES);  // [GRP][HD + 2]: o, running max, sum
+  // per head: o [GRP][HD], then (running max, sum) [GRP][2]
+  float *part = reinterpret_cast<float *>(sm + DNST * TL::BYTES);
   cg::cluster_group cl = cg::this_cluster();
   const int cs = (int)cl.num_blocks(), sp = (int)cl.block_rank();
   const int g = blockIdx.y, b = blockIdx.z;
@@ -198,6 +199,19 @@ __global__ void __launch_bounds__(GRP * 32, 1) k_attn_dec(AttnArgs a) {
 
   pdl_wait();
   pdl_trigger();
+
+  // K/V of position p itself (written by the QKV kernel this kernel follows),
+  // folded in by the last split after its tiles: loaded now, with q, so the
+  // round trip overlaps the tile loop
+  float kp[PER], vp[PER];
+  if (sp == cs - 1) {
+    const uint16_t *kc = Kb + (size_t)p * HD + lane * PER, *vc = Vb + (size_t)p * HD + lane * PER;
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+      kp[r] = act_to_f(kc[r], ACT);
+      vp[r] = act_to_f(vc[r], ACT);
+    }
+  }
 
   // q of head h as 16-bit pairs (q is act-rounded after RoPE: exact)
   const int h = g * GRP + warp;
@@ -266,41 +280,61 @@ __global__ void __launch_bounds__(GRP * 32, 1) k_attn_dec(AttnArgs a) {
   // position p itself (its K/V were written by the QKV kernel this kernel
   // follows): folded in by the last split
   if (sp == cs - 1) {
-    const uint16_t *kc = Kb + (size_t)p * HD + lane * PER, *vc = Vb + (size_t)p * HD + lane * PER;
     float d = 0.f;
 #pragma unroll
-    for (int r = 0; r < PER; ++r) d = fmaf(qp[lane * PER + r], act_to_f(kc[r], ACT), d);
+    for (int r = 0; r < PER; ++r) d = fmaf(qp[lane * PER + r], kp[r], d);
     const float sc = warp_sum(d) * scale;
     const float mnew = fmaxf(mrun, sc);
     const float corr = mrun == -INFINITY ? 0.f : expf(mrun - mnew), pe = expf(sc - mnew);
     lrun = lrun * corr + pe;
 #pragma unroll
-    for (int r = 0; r < PER; ++r) o[r] = fmaf(pe, act_to_f(vc[r], ACT), o[r] * corr);
+    for (int r = 0; r < PER; ++r) o[r] = fmaf(pe, vp[r], o[r] * corr);
     mrun = mnew;
   }
 
-  // merge across the cluster: split sp combines dims [sp * HD / cs, ...) of every head
-  float *pp = part + warp * (HD + 2);
+  // merge across the cluster: split sp combines dims [sp * HD / cs, ...) of
+  // every head.  Warp hh takes head hh; lane l < HD / 4 reads split
+  // r = l % cs (its max, sum and 4 dims of o, from that block's shared
+  // memory), so all the remote loads are in flight at once, and the cs lanes
+  // of a 4-dim block combine by shuffles.
+  float *pm = part + GRP * HD;
 #pragma unroll
-  for (int r = 0; r < PER; ++r) pp[lane * PER + r] = o[r];
+  for (int r = 0; r < PER; ++r) part[warp * HD + lane * PER + r] = o[r];
   if (lane == 0) {
-    pp[HD] = mrun;
-    pp[HD + 1] = lrun;
+    pm[warp * 2] = mrun;
+    pm[warp * 2 + 1] = lrun;
   }
   cl.sync();
-  const int dpc = HD / cs;
-  for (int e = tid; e < GRP * dpc; e += NT) {
-    const int hh = e / dpc, dd = sp * dpc + (e - hh * dpc);
-    float M = -INFINITY;
-    for (int r = 0; r < cs; ++r) M = fmaxf(M, cl.map_shared_rank(part, r)[hh * (HD + 2) + HD]);
-    float Ls = 0.f, O = 0.f;
-    for (int r = 0; r < cs; ++r) {
-      const float *rp = cl.map_shared_rank(part, r) + hh * (HD + 2);
-      const float w = rp[HD] == -INFINITY ? 0.f : expf(rp[HD] - M);
-      Ls = fmaf(w, rp[HD + 1], Ls);
-      O = fmaf(w, rp[dd], O);
+  {
+    const int dpc = HD / cs, r = lane % cs, d0 = sp * dpc + (lane / cs) * 4;
+    const bool live = lane < HD / 4;
+    float m = -INFINITY, l = 0.f;
+    float4 ov = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) {
+      const float *rp = cl.map_shared_rank(part, r);
+      m = rp[GRP * HD + warp * 2];
+      l = rp[GRP * HD + warp * 2 + 1];
+      ov = *reinterpret_cast<const float4 *>(rp + warp * HD + d0);
     }
-    a.o[((size_t)b * a.H + g * GRP + hh) * HD + dd] = round_act(O * (1.0f / Ls), ACT);
+    float M = m;
+    for (int x = 1; x < cs; x <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+    const float w = m == -INFINITY ? 0.f : expf(m - M);
+    float Ls = w * l, o0 = w * ov.x, o1 = w * ov.y, o2 = w * ov.z, o3 = w * ov.w;
+    for (int x = 1; x < cs; x <<= 1) {
+      Ls += __shfl_xor_sync(0xffffffffu, Ls, x);
+      o0 += __shfl_xor_sync(0xffffffffu, o0, x);
+      o1 += __shfl_xor_sync(0xffffffffu, o1, x);
+      o2 += __shfl_xor_sync(0xffffffffu, o2, x);
+      o3 += __shfl_xor_sync(0xffffffffu, o3, x);
+    }
+    if (live && r == 0) {
+      const float inv = 1.0f / Ls;
+      float *dst = a.o + ((size_t)b * a.H + g * GRP + warp) * HD + d0;
+      dst[0] = round_act(o0 * inv, ACT);
+      dst[1] = round_act(o1 * inv, ACT);
+      dst[2] = round_act(o2 * inv, ACT);
+      dst[3] = round_act(o3 * inv, ACT);
+    }
   }
   cl.sync();  // every split's partials stay readable until all merges are done
 }

@@ -46,14 +46,24 @@ __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
   pdl_wait();
   pdl_trigger();
   float ss = -1.f;  // sum of h^2, shared by the decision and the RMSNorm prologue
+  NormRegs nr;
+  bool have_nr = false;
   if ((EPI == EPI_QKV || EPI == EPI_LOGITS) && a.decide_layer1 > 0) {
     float dot = 0.f, n1 = 0.f, n2 = 0.f;
-    for (int i = tid * 4; i < a.m.K; i += blockDim.x * 4) {
-      const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.h_prev + i));
-      const float4 y = __ldcg(reinterpret_cast<const float4 *>(a.h + i));
-      dot = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, dot))));
-      n1 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, n1))));
-      n2 = fmaf(y.x, y.x, fmaf(y.y, y.y, fmaf(y.z, y.z, fmaf(y.w, y.w, n2))));
+    if (norm_fits(g)) {  // h and h_prev read once, kept for the RMSNorm prologue
+      norm_load<true>(a, g, a.h_prev, nr);
+      dot = nr.dot;
+      n1 = nr.n1;
+      n2 = nr.ss;
+      have_nr = true;
+    } else {
+      for (int i = tid * 4; i < a.m.K; i += blockDim.x * 4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.h_prev + i));
+        const float4 y = __ldcg(reinterpret_cast<const float4 *>(a.h + i));
+        dot = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, dot))));
+        n1 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, n1))));
+        n2 = fmaf(y.x, y.x, fmaf(y.y, y.y, fmaf(y.z, y.z, fmaf(y.w, y.w, n2))));
+      }
     }
     const float3 t = block_sum3(dot, n1, n2, bsum);
     dot = t.x;
@@ -69,7 +79,8 @@ __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
       is = gemv_begin<NW, EPI>(a, river, ring, blockIdx.x, gridDim.x);
     }
   }
-  PhaseOut o = gemv_run<NW, ACT, PRO, EPI>(a, river, smem, scratch, ring, is, blockIdx.x, gridDim.x, ss);
+  PhaseOut o = gemv_run<NW, ACT, PRO, EPI>(a, river, smem, scratch, ring, is, blockIdx.x, gridDim.x, ss,
+                                           have_nr ? &nr : nullptr);
 
   if (EPI == EPI_DOWN) {
     (void)o;  // the next QKV (or the LM head) makes this layer's exit decision

@@ -157,22 +157,45 @@ __host__ __device__ __forceinline__ size_t smem_bytes(const Geo &g, int nwarp) {
 // Activation prologue: x = round16(RMSNorm(h) * gamma) (PRO_NORM, r the
 // reciprocal RMS) or x = vec, staged in shared memory as 16-bit pairs in the
 // layout of the path.  Thread t of a pass handles the 8 activations
-// x[8t..8t+8), so a warp's loads cover 1 KB of contiguous fp32; every thread
-// issues the loads of SB passes before it converts and stores, so the
-// L2 round trips overlap instead of running one after the other.
+// x[8t..8t+8), so a warp's loads cover 1 KB of contiguous fp32.
 //   16-bit path: word t (= chunk c * 32 + lane) holds x[8t..8t+8) as 4 pairs.
 //   int4 path:   chunk c, lane ln, word j of the lane's 32-code run, t =
 //                c * 128 + ln * 4 + j: the pairs (x[8t+p], x[8t+p+4]); and per
 //                lane run the sum X of its 32 activations (4 words, summed by
 //                a 4-lane shuffle).
+// Word counts of the two layouts (multiples of 32, so warps stay converged).
+__host__ __device__ __forceinline__ int x_words(const Geo &g, int river) { return river ? g.nk4 * 128 : g.nk16 * 32; }
+
+// Store word t of x (8 values, already 16-bit-rounded where required).
+template <int ACT>
+__device__ __forceinline__ void store_xword(int river, int nk, int t, const float *x, float *xs) {
+  uint4 *xw = reinterpret_cast<uint4 *>(xs);
+  if (river) {
+    uint32_t pr[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) pr[q] = (uint32_t)f_to_act(x[q], ACT) | ((uint32_t)f_to_act(x[q + 4], ACT) << 16);
+    const int c = t >> 7, ln = (t >> 2) & 31, j = t & 3;
+    xw[(c * 4 + j) * 32 + ln] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+    float X = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+    X += __shfl_xor_sync(0xffffffffu, X, 1);
+    X += __shfl_xor_sync(0xffffffffu, X, 2);
+    if (j == 0) xs[nk * 4 * 32 * 4 + c * 32 + ln] = X;
+  } else {
+    xw[t] = make_uint4((uint32_t)f_to_act(x[0], ACT) | ((uint32_t)f_to_act(x[1], ACT) << 16),
+                       (uint32_t)f_to_act(x[2], ACT) | ((uint32_t)f_to_act(x[3], ACT) << 16),
+                       (uint32_t)f_to_act(x[4], ACT) | ((uint32_t)f_to_act(x[5], ACT) << 16),
+                       (uint32_t)f_to_act(x[6], ACT) | ((uint32_t)f_to_act(x[7], ACT) << 16));
+  }
+}
+
+// General prologue: every thread issues the loads of SB passes before it
+// converts and stores, so the L2 round trips of the passes overlap.
 template <int ACT, int PRO>
 __device__ __forceinline__ void stage_x(const GemvArgs &a, const Geo &g, int river, int nk, float r, float *xs) {
   constexpr int SB = 4;
-  const int nt = river ? nk * 128 : nk * 32;  // a multiple of 32: warps stay converged
+  const int nt = x_words(g, river);
   const float *src = PRO == PRO_NORM ? a.h : a.vec;
-  uint4 *xw = reinterpret_cast<uint4 *>(xs);
-  float *xsum = xs + nk * 4 * 32 * 4;
-  const int nthr = (int)blockDim.x;
+  const int nthr = (int)blockDim.x, lane = (int)(threadIdx.x & 31);
   for (int t0 = (int)threadIdx.x; t0 < nt; t0 += SB * nthr) {
     float4 u[SB][2];
     uint4 gw[SB];
@@ -192,31 +215,80 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const Geo &g, int riv
 #pragma unroll
     for (int i = 0; i < SB; ++i) {
       const int t = t0 + i * nthr;
-      if (t0 + i * nthr - (int)(threadIdx.x & 31) >= nt) break;  // the whole warp is past the end
+      if (t - lane >= nt) break;  // the whole warp is past the end
       float x[8] = {u[i][0].x, u[i][0].y, u[i][0].z, u[i][0].w, u[i][1].x, u[i][1].y, u[i][1].z, u[i][1].w};
       if (PRO == PRO_NORM) {
         const uint16_t *gp = reinterpret_cast<const uint16_t *>(&gw[i]);
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[j] = round_act(x[j] * r * act_to_f(gp[j], ACT), ACT);
       }
-      if (river) {
-        uint32_t pr[4];
+      store_xword<ACT>(river, nk, t, x, xs);
+    }
+  }
+}
+
+// RMSNorm prologue in one L2 round trip, for K up to NR_W * 8 * blockDim.x
+// (both layouts' words fit): the thread's words t = tid + i * blockDim.x of h,
+// of gamma and, where the exit decision is taken in the same prologue, of
+// h_prev are loaded into registers once; the RMSNorm sum (and the decision's
+// sums) come from them, then stage_norm writes x from them in the layout of
+// the route the decision picked.
+constexpr int NR_W = 2;
+struct NormRegs {
+  float4 h[NR_W][2];
+  uint4 gw[NR_W];
+  float ss, dot, n1;  // this thread's partial h.h, h_prev.h, h_prev.h_prev
+};
+
+__device__ __forceinline__ bool norm_fits(const Geo &g) {
+  return max(x_words(g, 0), x_words(g, 1)) <= NR_W * (int)blockDim.x;
+}
+
+template <bool DEC>
+__device__ __forceinline__ void norm_load(const GemvArgs &a, const Geo &g, const float *hprev, NormRegs &r) {
+  r.ss = r.dot = r.n1 = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          pr[q] = (uint32_t)f_to_act(x[q], ACT) | ((uint32_t)f_to_act(x[q + 4], ACT) << 16);
-        const int c = t >> 7, ln = (t >> 2) & 31, j = t & 3;
-        xw[(c * 4 + j) * 32 + ln] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-        float X = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
-        X += __shfl_xor_sync(0xffffffffu, X, 1);
-        X += __shfl_xor_sync(0xffffffffu, X, 2);
-        if (j == 0) xsum[c * 32 + ln] = X;
-      } else {
-        xw[t] = make_uint4((uint32_t)f_to_act(x[0], ACT) | ((uint32_t)f_to_act(x[1], ACT) << 16),
-                           (uint32_t)f_to_act(x[2], ACT) | ((uint32_t)f_to_act(x[3], ACT) << 16),
-                           (uint32_t)f_to_act(x[4], ACT) | ((uint32_t)f_to_act(x[5], ACT) << 16),
-                           (uint32_t)f_to_act(x[6], ACT) | ((uint32_t)f_to_act(x[7], ACT) << 16));
+  for (int i = 0; i < NR_W; ++i) {
+    const int t = (int)threadIdx.x + i * (int)blockDim.x;
+    r.h[i][0] = r.h[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    r.gw[i] = make_uint4(0u, 0u, 0u, 0u);
+    float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0;
+    if (t * 8 < g.K) {
+      const float4 *sp = reinterpret_cast<const float4 *>(a.h + t * 8);
+      r.h[i][0] = __ldcg(sp);
+      r.h[i][1] = __ldcg(sp + 1);
+      r.gw[i] = *reinterpret_cast<const uint4 *>(a.gamma + t * 8);
+      if (DEC) {
+        const float4 *pp = reinterpret_cast<const float4 *>(hprev + t * 8);
+        p0 = __ldcg(pp);
+        p1 = __ldcg(pp + 1);
       }
     }
+    const float4 y0 = r.h[i][0], y1 = r.h[i][1];
+    r.ss = fmaf(y0.x, y0.x, fmaf(y0.y, y0.y, fmaf(y0.z, y0.z, fmaf(y0.w, y0.w, r.ss))));
+    r.ss = fmaf(y1.x, y1.x, fmaf(y1.y, y1.y, fmaf(y1.z, y1.z, fmaf(y1.w, y1.w, r.ss))));
+    if (DEC) {
+      r.dot = fmaf(p0.x, y0.x, fmaf(p0.y, y0.y, fmaf(p0.z, y0.z, fmaf(p0.w, y0.w, r.dot))));
+      r.dot = fmaf(p1.x, y1.x, fmaf(p1.y, y1.y, fmaf(p1.z, y1.z, fmaf(p1.w, y1.w, r.dot))));
+      r.n1 = fmaf(p0.x, p0.x, fmaf(p0.y, p0.y, fmaf(p0.z, p0.z, fmaf(p0.w, p0.w, r.n1))));
+      r.n1 = fmaf(p1.x, p1.x, fmaf(p1.y, p1.y, fmaf(p1.z, p1.z, fmaf(p1.w, p1.w, r.n1))));
+    }
+  }
+}
+
+template <int ACT>
+__device__ __forceinline__ void stage_norm(const Geo &g, int river, int nk, float r, const NormRegs &nr, float *xs) {
+  const int nt = x_words(g, river), lane = (int)(threadIdx.x & 31);
+#pragma unroll
+  for (int i = 0; i < NR_W; ++i) {
+    const int t = (int)threadIdx.x + i * (int)blockDim.x;
+    if (t - lane >= nt) break;  // the whole warp is past the end
+    const float4 y0 = nr.h[i][0], y1 = nr.h[i][1];
+    float x[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+    const uint16_t *gp = reinterpret_cast<const uint16_t *>(&nr.gw[i]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = round_act(x[j] * r * act_to_f(gp[j], ACT), ACT);
+    store_xword<ACT>(river, nk, t, x, xs);
   }
 }
 
@@ -346,10 +418,12 @@ __device__ __forceinline__ ItemStream gemv_begin(const GemvArgs &a, int river, c
 // (x = round16(RMSNorm(h) * gamma) or x = vec, into the lane layout in xs),
 // the quad loop over the ring, and the epilogue in the owning warp.
 // scratch: 256 floats (cross-warp partials, block sums).
-// ss_in: sum of h^2 when the caller already has it (PRO_NORM), else < 0.
+// ss_in: sum of h^2 when the caller already has it (PRO_NORM), else < 0;
+// nrp: h already in registers (norm_load), ss_in then its block sum.
 template <int NWARP, int ACT, int PRO, int EPI>
 __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float *xs, float *scratch, char *ring,
-                                             ItemStream is, int bid, int nblocks, float ss_in = -1.f) {
+                                             ItemStream is, int bid, int nblocks, float ss_in = -1.f,
+                                             const NormRegs *nrp = nullptr) {
   if (!a.m.w) river = 1;  // an offloaded backbone layer exists only in the river
   const PhaseGeo p = phase_geo<NWARP>(a, river);
   const Geo &g = p.g;
@@ -358,20 +432,30 @@ __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float
   float *red = scratch;         // [2][NWARP * 4]: cross-warp partials, double-buffered
   float *bsum = scratch + 128;  // block_sum scratch (3 x 32)
 
-  float rs = 0.f;
-  if (PRO == PRO_NORM) {
-    float ss = ss_in;
-    if (ss < 0.f) {
-      ss = 0.f;
-      for (int i = tid * 4; i < g.K; i += blockDim.x * 4) {
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.h + i));
-        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+  if (PRO == PRO_NORM && nrp) {
+    // h (and the sums) already in registers: the caller took the exit decision from them
+    stage_norm<ACT>(g, river, nk, 1.0f / sqrtf(ss_in / (float)g.K + a.eps), *nrp, xs);
+  } else if (PRO == PRO_NORM && ss_in < 0.f && norm_fits(g)) {
+    NormRegs nr;
+    norm_load<false>(a, g, nullptr, nr);
+    const float ss = block_sum(nr.ss, bsum);
+    stage_norm<ACT>(g, river, nk, 1.0f / sqrtf(ss / (float)g.K + a.eps), nr, xs);
+  } else {
+    float rs = 0.f;
+    if (PRO == PRO_NORM) {
+      float ss = ss_in;
+      if (ss < 0.f) {
+        ss = 0.f;
+        for (int i = tid * 4; i < g.K; i += blockDim.x * 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.h + i));
+          ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+        }
+        ss = block_sum(ss, bsum);
       }
-      ss = block_sum(ss, bsum);
+      rs = 1.0f / sqrtf(ss / (float)g.K + a.eps);
     }
-    rs = 1.0f / sqrtf(ss / (float)g.K + a.eps);
+    stage_x<ACT, PRO>(a, g, river, nk, rs, xs);
   }
-  stage_x<ACT, PRO>(a, g, river, nk, rs, xs);
   __syncthreads();
 
   const int pos = (EPI == EPI_QKV) ? a.st.len[0] : 0;
