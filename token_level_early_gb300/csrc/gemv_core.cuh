@@ -121,6 +121,9 @@ __device__ __forceinline__ bool last_block(unsigned *counter) {
 struct Geo {
   int K, Kp, nk4, nk16, words, G;
   int gpc;  // groups per int4 chunk when the group size divides the chunk, else 0
+  int spr;  // 16-byte pieces of one row's (scale, zero) words per chunk, when
+            // they can be copied as such (gpc a multiple of 4, rows 16-byte
+            // aligned); else 0 and every lane copies its own group's word
 };
 
 __host__ __device__ __forceinline__ Geo geo_of(const Mat &m) {
@@ -132,6 +135,7 @@ __host__ __device__ __forceinline__ Geo geo_of(const Mat &m) {
   g.words = g.Kp >> 3;
   g.G = m.r.G;
   g.gpc = (m.r.g > 0 && CH4 % m.r.g == 0) ? CH4 / m.r.g : 0;
+  g.spr = (g.gpc >= 4 && g.gpc % 4 == 0 && g.G % 4 == 0) ? g.gpc / 4 : 0;
   return g;
 }
 
@@ -334,18 +338,26 @@ __device__ __forceinline__ void issue_item(const GemvArgs &a, const Geo &g, int 
       const int k0 = is.c * CH4 + lane * 32;
       if (k0 < g.Kp) {
         const uint32_t *qb = a.m.r.q + (k0 >> 3);
-        const __half2 *sb = a.m.r.sz + (g.gpc ? is.c * g.gpc + lane_g : k0 / a.m.r.g);
-        const unsigned ss = (unsigned)__cvta_generic_to_shared(stage) + STAGE_W + lane * 4;
         const uint32_t *q0 = qb + is.off0, *q2 = qb + is.off2;
-        const __half2 *s0 = sb + is.soff0, *s2 = sb + is.soff2;
         cp16s(sd, q0);
         cp16s(sd + 512, q0 + g.words);
         cp16s(sd + 1024, q2);
         cp16s(sd + 1536, q2 + g.words);
-        cp4s(ss, s0);
-        cp4s(ss + 128, s0 + g.G);
-        cp4s(ss + 256, s2);
-        cp4s(ss + 384, s2 + g.G);
+        if (!g.spr) {  // each lane its own group's word: row r at r * 32 + lane
+          const __half2 *sb = a.m.r.sz + (g.gpc ? is.c * g.gpc + lane_g : k0 / a.m.r.g);
+          const unsigned ss = (unsigned)__cvta_generic_to_shared(stage) + STAGE_W + lane * 4;
+          const __half2 *s0 = sb + is.soff0, *s2 = sb + is.soff2;
+          cp4s(ss, s0);
+          cp4s(ss + 128, s0 + g.G);
+          cp4s(ss + 256, s2);
+          cp4s(ss + 384, s2 + g.G);
+        }
+      }
+      if (g.spr && lane < 4 * g.spr) {  // the chunk's groups of the 4 rows: row r at r * gpc
+        const int r = lane / g.spr, piece = lane - r * g.spr;
+        if (is.c * g.gpc + piece * 4 < g.G)  // a ragged last chunk has fewer groups
+          cp16s((unsigned)__cvta_generic_to_shared(stage) + STAGE_W + (r * g.gpc + piece * 4) * 4,
+                a.m.r.sz + (r < 2 ? is.soff0 : is.soff2) + (r & 1) * g.G + is.c * g.gpc + piece * 4);
       }
     } else {
       const int k0 = is.c * CH16 + lane * 8;
@@ -485,6 +497,7 @@ __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float
           const uint4 *xq = reinterpret_cast<const uint4 *>(xs) + c * 4 * 32 + lane;
           const float X = xs[nk * 4 * 32 * 4 + c * 32 + lane];
           const __half2 *ss = reinterpret_cast<const __half2 *>(stg + STAGE_W);
+          const int srow = g.spr ? g.gpc : 32, sidx = g.spr ? p.lane_g : lane;
           uint32_t xr[16];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -499,7 +512,7 @@ __device__ __forceinline__ PhaseOut gemv_run(const GemvArgs &a, int river, float
             word_mix<ACT>(w.y, xr + 4, a0, a1, cm, c1);
             word_mix<ACT>(w.z, xr + 8, a0, a1, cm, c1);
             word_mix<ACT>(w.w, xr + 12, a0, a1, cm, c1);
-            const float2 sz = __half22float2(ss[r * 32 + lane]);
+            const float2 sz = __half22float2(ss[r * srow + sidx]);
             const float run = fmaf(CodeBits<ACT>::A, a0 + a1, -(CodeBits<ACT>::B + sz.y) * X);
             v[r] = fmaf(sz.x, run, v[r]);
           }
