@@ -116,13 +116,30 @@ __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
 
 // ------------------------------------------------------------------ launch
 
+// K splits per row quad (S warps of a block share a quad's chunks; 1, 2, 4
+// or 8): the choice that gives the busiest warp of the launch the fewest work
+// items, with at most grid_cap blocks; ties go to fewer splits (fewer
+// cross-warp reductions).
+static int best_splits(int nq, int nk, int grid_cap) {
+  int best = 1;
+  long best_cost = -1;
+  for (int S = 1; S <= 8 && S <= nk; S *= 2) {
+    const long iters = (nq + NW / S - 1) / (NW / S);  // block iterations of RG = NW / S quads
+    const long grid = iters < grid_cap ? iters : grid_cap;
+    const long cost = (iters + grid - 1) / grid * ((nk + S - 1) / S);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
+}
+
 template <int ACT, int PRO, int EPI>
 static cudaError_t launch_t(const GemvArgs &a_in, int max_grid, cudaStream_t s, int pdl) {
   GemvArgs a = a_in;
   const Geo g = geo_of(a.m);
   const int nq = a.m.N / 4;
-  a.s4 = splits_for(nq, g.nk4);
-  a.s16 = splits_for(nq, g.nk16);
   const size_t smem = smem_bytes(g, NW);
   auto fn = k_gemv_b1<ACT, PRO, EPI>;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
@@ -130,19 +147,22 @@ static cudaError_t launch_t(const GemvArgs &a_in, int max_grid, cudaStream_t s, 
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  // Enough blocks for the path with more (quad, split) groups, never beyond
-  // one resident wave; the grid-stride loop covers the rest.
-  const int s_max = a.s4 > a.s16 ? a.s4 : a.s16;
-  const int RG = NW / s_max;
-  int grid = (nq + RG - 1) / RG;
   int per_sm = 0, dev = 0, n_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, NW * 32, smem);
   if (e != cudaSuccess) return e;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (per_sm < 1) per_sm = 1;
-  if (grid > per_sm * n_sm) grid = per_sm * n_sm;
-  if (grid > max_grid) grid = max_grid;
+  // never beyond one resident wave; the grid-stride loop covers the rest
+  int cap = per_sm * n_sm;
+  if (cap > max_grid) cap = max_grid;
+  a.s4 = best_splits(nq, g.nk4, cap);
+  a.s16 = best_splits(nq, g.nk16, cap);
+  // enough blocks for the path with more block iterations
+  const int s_max = a.s4 > a.s16 ? a.s4 : a.s16;
+  const int RG = NW / s_max;
+  int grid = (nq + RG - 1) / RG;
+  if (grid > cap) grid = cap;
   return launch_k(fn, dim3(grid), dim3(NW * 32), smem, s, pdl, a);
 }
 
