@@ -100,6 +100,7 @@ struct rv_model {
   // batch-1 activations
   float *hbuf[2] = {nullptr, nullptr}, *hmid = nullptr, *qbuf = nullptr, *obuf = nullptr, *abuf = nullptr;
   float *partials = nullptr;
+  unsigned *seq_min = nullptr;  // [Bmax] prefill sequence-exit minima (order-preserving encoding)
   unsigned *counters = nullptr;
   int attn_splits_b1 = 1, attn_splits_max = 1, attn_cluster = 1;
   float *attn_part = nullptr;
@@ -651,6 +652,8 @@ static int load_impl(rv_model *m, const rv_config *cfg, const void *const *weigh
   RV_ALLOC(A, m->obuf, sizeof(float) * m->qd);
   RV_ALLOC(A, m->abuf, sizeof(float) * F);
   RV_ALLOC(A, m->partials, sizeof(float) * 3 * 4 * (size_t)m->n_sm);
+  RV_ALLOC(A, m->seq_min, sizeof(unsigned) * (size_t)m->Bmax);
+  RV_CK(cudaMemsetAsync(m->seq_min, 0xFF, sizeof(unsigned) * (size_t)m->Bmax, m->stream));
   RV_ALLOC(A, m->counters, sizeof(unsigned) * (m->L + 4));
   RV_CK(cudaMemsetAsync(m->counters, 0, sizeof(unsigned) * (m->L + 4), m->stream));
   int sp = (2 * m->n_sm + m->Hkv - 1) / m->Hkv;
@@ -899,7 +902,7 @@ int rv_prefill(rv_model *m, const int32_t *tokens, int B, int T0, float tau, int
   for (int l = 0; l < m->L; ++l) {
     rc = enqueue_layer_rows(m, l, B, T0, nullptr, s);
     if (rc) return rc;
-    RV_CK(launch_seq_decide(m->st, m->gHin, m->gH, m->d, B, T0, l + 1, m->L, fixed_exit_layer,
+    RV_CK(launch_seq_decide(m->st, m->gHin, m->gH, m->d, B, T0, l + 1, m->L, fixed_exit_layer, m->seq_min,
                             m->debug ? m->dbg_s + (size_t)l * m->Bmax : nullptr, s));
     if (m->debug)
       RV_CK(launch_copy_rows(m->gH + (size_t)(T0 - 1) * m->d, T0 * m->d, m->dbg_h + (size_t)(l + 1) * m->Bmax * m->d,

@@ -211,16 +211,28 @@ cudaError_t launch_decide_rows(const StepState &st, const float *Hin, const floa
 
 // Sequence-level decision for prefill: exit when min over the sequence's
 // tokens of s_t(l) exceeds tau (the latest-exiting token sets the depth).
-__global__ void k_seq_decide(StepState st, const float *Hin, const float *H, int d, int T, int layer1, int L,
-                             int fixed_exit, float *dbg_smin) {
+// Pass 1 spreads the tokens over the GPU (a warp per token, the same sums in
+// the same order as a single-block pass would take) and folds each block's
+// minimum into smin[b], a float in an order-preserving unsigned encoding (min
+// is exact, so the result does not depend on the order of the atomics).
+// Pass 2 decides and re-arms smin[b] for the next layer.
+__device__ __forceinline__ unsigned f2ord(float f) {
+  const unsigned u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ord2f(unsigned o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+constexpr int SEQ_TOK_PER_BLOCK = 64;
+
+__global__ void k_seq_smin(StepState st, const float *Hin, const float *H, int d, int T, unsigned *smin) {
   __shared__ float wmin[32];
-  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  if (st.route[b] != 0) {
-    if (threadIdx.x == 0 && dbg_smin) dbg_smin[b] = __int_as_float(0x7fc00000);
-    return;
-  }
+  const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  if (st.route[b] != 0) return;
+  const int t0 = blockIdx.x * SEQ_TOK_PER_BLOCK, t1 = min(T, t0 + SEQ_TOK_PER_BLOCK);
   float mn = INFINITY;
-  for (int t = warp; t < T; t += nw) {
+  for (int t = t0 + warp; t < t1; t += nw) {
     const float *x = Hin + ((size_t)b * T + t) * d, *y = H + ((size_t)b * T + t) * d;
     float dot = 0.f, n1 = 0.f, n2 = 0.f;
     for (int i = lane; i < d; i += 32) {
@@ -239,6 +251,20 @@ __global__ void k_seq_decide(StepState st, const float *Hin, const float *H, int
   if (threadIdx.x != 0) return;
   for (int w = 1; w < nw; ++w) mn = fminf(mn, wmin[w]);
   mn = fminf(mn, wmin[0]);
+  atomicMin(smin + b, f2ord(mn));
+}
+
+__global__ void k_seq_decide(StepState st, int B, int layer1, int L, int fixed_exit, unsigned *smin,
+                             float *dbg_smin) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const unsigned o = smin[b];
+  smin[b] = 0xFFFFFFFFu;  // re-armed for the next layer
+  if (st.route[b] != 0) {
+    if (dbg_smin) dbg_smin[b] = __int_as_float(0x7fc00000);
+    return;
+  }
+  const float mn = o == 0xFFFFFFFFu ? INFINITY : ord2f(o);  // no token: as the empty minimum
   if (dbg_smin) dbg_smin[b] = mn;
   bool go;
   if (fixed_exit >= 0)
@@ -253,8 +279,13 @@ __global__ void k_seq_decide(StepState st, const float *Hin, const float *H, int
 }
 
 cudaError_t launch_seq_decide(const StepState &st, const float *Hin, const float *H, int d, int B, int T,
-                              int layer1, int L, int fixed_exit, float *dbg_smin, cudaStream_t s) {
-  k_seq_decide<<<B, 256, 0, s>>>(st, Hin, H, d, T, layer1, L, fixed_exit, dbg_smin);
+                              int layer1, int L, int fixed_exit, unsigned *smin, float *dbg_smin, cudaStream_t s) {
+  if (T > 0) {
+    k_seq_smin<<<dim3((T + SEQ_TOK_PER_BLOCK - 1) / SEQ_TOK_PER_BLOCK, B), 256, 0, s>>>(st, Hin, H, d, T, smin);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  k_seq_decide<<<(B + 127) / 128, 128, 0, s>>>(st, B, layer1, L, fixed_exit, smin, dbg_smin);
   return cudaGetLastError();
 }
 

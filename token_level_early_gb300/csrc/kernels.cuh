@@ -149,8 +149,9 @@ cudaError_t launch_swiglu_rows(const float *Y, int F, int act, float *A, const i
                                const int32_t *count, int max_rows, cudaStream_t s);
 cudaError_t launch_decide_rows(const StepState &st, const float *Hin, const float *H, int d, int B, int layer1,
                                int L, float *dbg_s, cudaStream_t s);
+// smin: B unsigned words, all 0xFFFFFFFF before the first call (each call leaves them so).
 cudaError_t launch_seq_decide(const StepState &st, const float *Hin, const float *H, int d, int B, int T,
-                              int layer1, int L, int fixed_exit, float *dbg_smin, cudaStream_t s);
+                              int layer1, int L, int fixed_exit, unsigned *smin, float *dbg_smin, cudaStream_t s);
 cudaError_t launch_argmax_rows(const float *logits, int V, int B, StepState st, int bump_len, int set_len,
                                cudaStream_t s);
 cudaError_t launch_copy_rows(const float *src, int src_stride, float *dst, int dst_stride, int d, int B,
