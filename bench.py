@@ -408,6 +408,19 @@ def run_reference(wl_name, steps, warmup, budget_s=150.0):
 
 # ------------------------------------------------------------------ main
 
+def layer_us(res, L):
+    """River vs backbone layer time (the analogue of the pages' 2.4x): the
+    all-river and full-backbone steps minus the LM head's own time, per
+    layer (the embedding and step set-up are a few microseconds)."""
+    m, k = res["modes"], res["kernels"]
+    if "full" not in m or "river" not in m or "lmhead_bf16" not in k:
+        return None
+    head = k["lmhead_bf16"]["ms"]
+    bb = (m["full"]["ms_per_step"] - head) * 1e3 / L
+    rv_ = (m["river"]["ms_per_step"] - head) * 1e3 / L
+    return {"backbone": bb, "river": rv_, "ratio": bb / rv_, "pages": "exit layers ~2.4x faster than backbone layers"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -506,6 +519,7 @@ def main():
             "modes": modes,
             "speedup_vs_full_backbone": (tau_r["tokens_per_s"] / res["modes"]["full"]["tokens_per_s"]
                                          if "full" in res["modes"] else None),
+            "layer_us": layer_us(res, L),
             "roofline": roof, "kernels": res["kernels"], "cpu_baseline": res["cpu"], "offload": res["offload"],
             "fidelity": fid,
             "e2e": {"value": world * e2e, "unit": "tokens/s", "h2d_bytes_per_step": 4 * 6,

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(GRP * 32) k_attn(AttnArgs a, int T_per_row, co
 
 // ---- decode: clustered split-KV attention ----------------------------------
 constexpr int DTT = 32;   // positions per tile (one per lane in the score pass)
-constexpr int DNST = 4;   // ring stages
+constexpr int DNST = 5;   // ring stages: a split of up to DNST - 1 tiles is in flight before the wait
 
 template <int HD>
 struct DecTile {
@@ -151,7 +151,40 @@ struct DecTile {
 
 template <int HD>
 static size_t dec_smem(int grp) {
-  return (size_t)DNST * DecTile<HD>::BYTES + sizeof(float) * grp * (HD + 2);
+  return (size_t)DNST * DecTile<HD>::BYTES + sizeof(float) * grp * (HD + 2) + sizeof(float) * grp * DNST * DTT;
+}
+
+// o[r] += sum over the tile's first n positions t of p[t] * V[t][lane * PER + r],
+// p broadcast from shared memory (all lanes read the same word); full tiles
+// unrolled with two accumulator sets to halve the dependent FMA chains.
+template <int HD, int ACT>
+__device__ __forceinline__ void v_accumulate(const unsigned char *tv, const float *pw, int n, int lane, float *o) {
+  constexpr int PER = HD / 32, VROW = HD * 2;
+  if (n == DTT) {
+    float e[PER];
+#pragma unroll
+    for (int r = 0; r < PER; ++r) e[r] = 0.f;
+#pragma unroll
+    for (int t = 0; t < DTT; t += 2) {
+      const float p0 = pw[t], p1 = pw[t + 1];
+      const uint16_t *v0 = reinterpret_cast<const uint16_t *>(tv + t * VROW) + lane * PER;
+      const uint16_t *v1 = v0 + HD;
+#pragma unroll
+      for (int r = 0; r < PER; ++r) {
+        o[r] = fmaf(p0, act_to_f(v0[r], ACT), o[r]);
+        e[r] = fmaf(p1, act_to_f(v1[r], ACT), e[r]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < PER; ++r) o[r] += e[r];
+  } else {
+    for (int t = 0; t < n; ++t) {
+      const float pt = pw[t];
+      const uint16_t *vr = reinterpret_cast<const uint16_t *>(tv + t * VROW) + lane * PER;
+#pragma unroll
+      for (int r = 0; r < PER; ++r) o[r] = fmaf(pt, act_to_f(vr[r], ACT), o[r]);
+    }
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_act2(float lo, float hi, int act) {
@@ -165,6 +198,7 @@ __global__ void __launch_bounds__(GRP * 32, 1) k_attn_dec(AttnArgs a) {
   extern __shared__ __align__(16) unsigned char sm[];
   // per head: o [GRP][HD], then (running max, sum) [GRP][2]
   float *part = reinterpret_cast<float *>(sm + DNST * TL::BYTES);
+  float *pbuf = part + GRP * (HD + 2);  // [GRP][DNST * DTT]: softmax numerators of the warp's positions
   cg::cluster_group cl = cg::this_cluster();
   const int cs = (int)cl.num_blocks(), sp = (int)cl.block_rank();
   const int g = blockIdx.y, b = blockIdx.z;
@@ -228,53 +262,94 @@ __global__ void __launch_bounds__(GRP * 32, 1) k_attn_dec(AttnArgs a) {
 #pragma unroll
   for (int r = 0; r < PER; ++r) o[r] = 0.f;
 
-  for (int tile = tb, it = 0; tile < te; ++tile, ++it) {
-    cp_wait<DNST - 2>();
-    __syncthreads();  // the tile is in; every warp is done with the slot refilled next
-    issue(tile + DNST - 1, (it + DNST - 1) % DNST);
-    const unsigned char *tk = sm + (it % DNST) * TL::BYTES;
-    const unsigned char *tv = tk + DTT * TL::KROW;
-    const int n = min(DTT, p - tile * DTT);
-    float sc = -INFINITY;
-    if (lane < n) {
-      const uint4 *kr = reinterpret_cast<const uint4 *>(tk + lane * TL::KROW);
-      float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+  if (te - tb <= DNST - 1) {
+    // Every tile of this split is in flight since before the wait: scores
+    // of all its positions first (lane j takes position j of each tile), one
+    // max and one sum, then the V pass with the final numerators.
+    cp_wait<0>();
+    __syncthreads();
+    const int nt = te - tb;
+    float sc[DNST - 1];
+    float mx = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < PR; ++j) {
-        const uint4 k = kr[j];
-        d0 = fma_lo16<ACT>(k.x, qr[4 * j], d0);
-        d1 = fma_hi16<ACT>(k.x, qr[4 * j], d1);
-        d2 = fma_lo16<ACT>(k.y, qr[4 * j + 1], d2);
-        d3 = fma_hi16<ACT>(k.y, qr[4 * j + 1], d3);
-        d0 = fma_lo16<ACT>(k.z, qr[4 * j + 2], d0);
-        d1 = fma_hi16<ACT>(k.z, qr[4 * j + 2], d1);
-        d2 = fma_lo16<ACT>(k.w, qr[4 * j + 3], d2);
-        d3 = fma_hi16<ACT>(k.w, qr[4 * j + 3], d3);
-      }
-      sc = ((d0 + d1) + (d2 + d3)) * scale;
-    }
-    const float mnew = fmaxf(mrun, warp_max(sc));
-    const float pe = lane < n ? expf(sc - mnew) : 0.f;
-    const float corr = mrun == -INFINITY ? 0.f : expf(mrun - mnew);
-    lrun = lrun * corr + warp_sum(pe);
+    for (int i = 0; i < DNST - 1; ++i) {
+      sc[i] = -INFINITY;
+      const int n = i < nt ? min(DTT, p - (tb + i) * DTT) : 0;
+      if (lane < n) {
+        const uint4 *kr = reinterpret_cast<const uint4 *>(sm + i * TL::BYTES + lane * TL::KROW);
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
 #pragma unroll
-    for (int r = 0; r < PER; ++r) o[r] *= corr;
-    for (int t = 0; t < n; ++t) {
-      const float pt = __shfl_sync(0xffffffffu, pe, t);
-      const uint16_t *vr = reinterpret_cast<const uint16_t *>(tv + t * TL::VROW) + lane * PER;
-      if constexpr (PER == 4) {
-        const uint2 vv = *reinterpret_cast<const uint2 *>(vr);
-        o[0] = fmaf(pt, act_to_f((uint16_t)(vv.x & 0xFFFFu), ACT), o[0]);
-        o[1] = fmaf(pt, act_to_f((uint16_t)(vv.x >> 16), ACT), o[1]);
-        o[2] = fmaf(pt, act_to_f((uint16_t)(vv.y & 0xFFFFu), ACT), o[2]);
-        o[3] = fmaf(pt, act_to_f((uint16_t)(vv.y >> 16), ACT), o[3]);
-      } else {
-        const uint32_t vv = *reinterpret_cast<const uint32_t *>(vr);
-        o[0] = fmaf(pt, act_to_f((uint16_t)(vv & 0xFFFFu), ACT), o[0]);
-        o[1] = fmaf(pt, act_to_f((uint16_t)(vv >> 16), ACT), o[1]);
+        for (int j = 0; j < PR; ++j) {
+          const uint4 k = kr[j];
+          d0 = fma_lo16<ACT>(k.x, qr[4 * j], d0);
+          d1 = fma_hi16<ACT>(k.x, qr[4 * j], d1);
+          d2 = fma_lo16<ACT>(k.y, qr[4 * j + 1], d2);
+          d3 = fma_hi16<ACT>(k.y, qr[4 * j + 1], d3);
+          d0 = fma_lo16<ACT>(k.z, qr[4 * j + 2], d0);
+          d1 = fma_hi16<ACT>(k.z, qr[4 * j + 2], d1);
+          d2 = fma_lo16<ACT>(k.w, qr[4 * j + 3], d2);
+          d3 = fma_hi16<ACT>(k.w, qr[4 * j + 3], d3);
+        }
+        sc[i] = ((d0 + d1) + (d2 + d3)) * scale;
       }
+      mx = fmaxf(mx, sc[i]);
     }
-    mrun = mnew;
+    mx = warp_max(mx);
+    float *pw = pbuf + warp * DNST * DTT;
+    float ls = 0.f;
+#pragma unroll
+    for (int i = 0; i < DNST - 1; ++i) {
+      const float pe = sc[i] == -INFINITY ? 0.f : expf(sc[i] - mx);
+      pw[i * DTT + lane] = pe;
+      ls += pe;
+    }
+    ls = warp_sum(ls);
+    __syncwarp();
+    for (int i = 0; i < nt; ++i)
+      v_accumulate<HD, ACT>(sm + i * TL::BYTES + DTT * TL::KROW, pw + i * DTT, min(DTT, p - (tb + i) * DTT), lane, o);
+    if (nt > 0) {
+      mrun = mx;
+      lrun = ls;
+    }
+  } else {
+    for (int tile = tb, it = 0; tile < te; ++tile, ++it) {
+      cp_wait<DNST - 2>();
+      __syncthreads();  // the tile is in; every warp is done with the slot refilled next
+      issue(tile + DNST - 1, (it + DNST - 1) % DNST);
+      const unsigned char *tk = sm + (it % DNST) * TL::BYTES;
+      const unsigned char *tv = tk + DTT * TL::KROW;
+      const int n = min(DTT, p - tile * DTT);
+      float sc = -INFINITY;
+      if (lane < n) {
+        const uint4 *kr = reinterpret_cast<const uint4 *>(tk + lane * TL::KROW);
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < PR; ++j) {
+          const uint4 k = kr[j];
+          d0 = fma_lo16<ACT>(k.x, qr[4 * j], d0);
+          d1 = fma_hi16<ACT>(k.x, qr[4 * j], d1);
+          d2 = fma_lo16<ACT>(k.y, qr[4 * j + 1], d2);
+          d3 = fma_hi16<ACT>(k.y, qr[4 * j + 1], d3);
+          d0 = fma_lo16<ACT>(k.z, qr[4 * j + 2], d0);
+          d1 = fma_hi16<ACT>(k.z, qr[4 * j + 2], d1);
+          d2 = fma_lo16<ACT>(k.w, qr[4 * j + 3], d2);
+          d3 = fma_hi16<ACT>(k.w, qr[4 * j + 3], d3);
+        }
+        sc = ((d0 + d1) + (d2 + d3)) * scale;
+      }
+      const float mnew = fmaxf(mrun, warp_max(sc));
+      const float pe = lane < n ? expf(sc - mnew) : 0.f;
+      const float corr = mrun == -INFINITY ? 0.f : expf(mrun - mnew);
+      lrun = lrun * corr + warp_sum(pe);
+#pragma unroll
+      for (int r = 0; r < PER; ++r) o[r] *= corr;
+      float *pw = pbuf + warp * DNST * DTT;
+      pw[lane] = pe;
+      __syncwarp();
+      v_accumulate<HD, ACT>(tv, pw, n, lane, o);
+      __syncwarp();  // pw is rewritten by the next tile
+      mrun = mnew;
+    }
   }
 
   // position p itself (its K/V were written by the QKV kernel this kernel
