@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
   float *bsum = scratch + 128;
   int river = (EPI == EPI_LOGITS) ? 0 : ld_relaxed_i32(a.st.route);
   ItemStream is = gemv_begin<NW, EPI>(a, river, ring, blockIdx.x, gridDim.x);
+  DecideScalars dsc{};
+  if ((EPI == EPI_QKV || EPI == EPI_LOGITS) && a.decide_layer1 > 0) dsc = load_decide_scalars(a.st, 0);
   pdl_wait();
   pdl_trigger();
   float ss = -1.f;  // sum of h^2, shared by the decision and the RMSNorm prologue
@@ -71,7 +73,7 @@ __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
     n2 = t.z;
     ss = n2;
     const int route_now = (EPI == EPI_LOGITS) ? a.st.route[0] : river;
-    const Decision dc = decide(a.st, 0, route_now, a.decide_layer1, a.L, dot, n1, n2);
+    const Decision dc = decide(dsc, route_now, a.decide_layer1, a.L, dot, n1, n2);
     if (blockIdx.x == 0 && tid == 0) commit_decision(a.st, 0, a.decide_layer1, dc, a.dbg_s);
     if (EPI == EPI_QKV && dc.route != river) {
       cp_wait<0>();  // drop the speculative items, then stream the river copy

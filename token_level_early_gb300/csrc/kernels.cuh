@@ -48,23 +48,44 @@ struct Decision {
   bool exited;
   float s;
 };
-__device__ __forceinline__ Decision decide(const StepState &st, int b, int route_now, int layer1, int L, float dot,
+// The step's decision inputs for row b, read once: a kernel of the batch-1
+// chain loads them before its dependency wait (they are written before the
+// step's first layer kernel), so the decision itself waits on no memory.
+struct DecideScalars {
+  int mode, forced, entry, cap;
+  float tau;
+};
+__device__ __forceinline__ DecideScalars load_decide_scalars(const StepState &st, int b) {
+  DecideScalars p;
+  p.mode = *st.mode;
+  p.forced = st.forced[b];
+  p.entry = *st.entry;
+  p.cap = *st.cap;
+  p.tau = *st.tau;
+  return p;
+}
+__device__ __forceinline__ Decision decide(const DecideScalars &p, int route_now, int layer1, int L, float dot,
                                            float n1, float n2) {
   Decision d{route_now, false, __int_as_float(0x7fc00000)};
   if (route_now != 0) return d;
   const float den = fmaxf(sqrtf(n1) * sqrtf(n2), 1e-8f);
   d.s = dot / den;
-  if (*st.mode == 1) {
-    int f = st.forced[b];
+  if (p.mode == 1) {
+    int f = p.forced;
     if (f < 0 || f > L) f = L;
     d.exited = layer1 == f && layer1 < L;
   } else {
-    d.exited = layer1 >= *st.entry && layer1 <= L - 1 && d.s > *st.tau;
+    d.exited = layer1 >= p.entry && layer1 <= L - 1 && d.s > p.tau;
   }
   // backbone offloading: the layers after the cap exist only in the river
-  if (layer1 >= *st.cap && layer1 < L) d.exited = true;
+  if (layer1 >= p.cap && layer1 < L) d.exited = true;
   if (d.exited) d.route = 1;
   return d;
+}
+__device__ __forceinline__ Decision decide(const StepState &st, int b, int route_now, int layer1, int L, float dot,
+                                           float n1, float n2) {
+  if (route_now != 0) return Decision{route_now, false, __int_as_float(0x7fc00000)};
+  return decide(load_decide_scalars(st, b), route_now, layer1, L, dot, n1, n2);
 }
 // Record a decision in the step state (one thread).
 __device__ __forceinline__ void commit_decision(const StepState &st, int b, int layer1, const Decision &d,
