@@ -24,6 +24,28 @@ namespace rv {
 
 constexpr int NW = 8;  // warps per block
 
+// Largest value, lowest index on ties, over the block (all threads return
+// the block's pair; sv, si: one slot per warp).
+__device__ __forceinline__ void block_argmax(float &v, int &i, float *sv, int *si) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();  // the slots may still be read from an earlier call
+  if (lane == 0) {
+    sv[warp] = v;
+    si[warp] = i;
+  }
+  __syncthreads();
+  v = sv[0];
+  i = si[0];
+  for (int w = 1; w < nw; ++w)
+    if (sv[w] > v || (sv[w] == v && si[w] < i)) { v = sv[w]; i = si[w]; }
+}
+
 template <int ACT, int PRO, int EPI>
 __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
   extern __shared__ __align__(16) float smem[];
@@ -87,29 +109,27 @@ __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
   if (EPI == EPI_DOWN) {
     (void)o;  // the next QKV (or the LM head) makes this layer's exit decision
   } else if (EPI == EPI_LOGITS) {
-    // block argmax (lowest index on ties)
-    __shared__ float bv[NW * 32];
-    __shared__ int bi[NW * 32];
-    bv[tid] = o.best;
-    bi[tid] = o.best_i;
-    __syncthreads();
+    // block argmax (lowest index on ties), then the last block to finish
+    // reduces the blocks' candidates: both by shuffles, no serial loops
+    __shared__ float bv[NW];
+    __shared__ int bi[NW];
+    float vb = o.best;
+    int ib = o.best_i;
+    block_argmax(vb, ib, bv, bi);
     if (tid == 0) {
-      float vb = bv[0];
-      int ib = bi[0];
-      for (int q = 1; q < NW * 32; ++q)
-        if (bv[q] > vb || (bv[q] == vb && bi[q] < ib)) { vb = bv[q]; ib = bi[q]; }
       a.partials[blockIdx.x * 2] = vb;
       reinterpret_cast<int *>(a.partials)[blockIdx.x * 2 + 1] = ib;
     }
     if (!last_block(a.counter)) return;
+    vb = -INFINITY;
+    ib = 0x7fffffff;
+    for (int b = tid; b < (int)gridDim.x; b += blockDim.x) {
+      const float bvv = __ldcg(a.partials + b * 2);
+      const int bii = __ldcg(reinterpret_cast<const int *>(a.partials) + b * 2 + 1);
+      if (bvv > vb || (bvv == vb && bii < ib)) { vb = bvv; ib = bii; }
+    }
+    block_argmax(vb, ib, bv, bi);
     if (tid == 0) {
-      float vb = -INFINITY;
-      int ib = 0x7fffffff;
-      for (int b = 0; b < (int)gridDim.x; ++b) {
-        const float bvv = a.partials[b * 2];
-        const int bii = reinterpret_cast<const int *>(a.partials)[b * 2 + 1];
-        if (bvv > vb || (bvv == vb && bii < ib)) { vb = bvv; ib = bii; }
-      }
       a.st.next_ids[0] = ib == 0x7fffffff ? 0 : ib;
       a.st.len[0] += 1;
     }
