@@ -24,28 +24,6 @@ namespace rv {
 
 constexpr int NW = 8;  // warps per block
 
-// Largest value, lowest index on ties, over the block (all threads return
-// the block's pair; sv, si: one slot per warp).
-__device__ __forceinline__ void block_argmax(float &v, int &i, float *sv, int *si) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  __syncthreads();  // the slots may still be read from an earlier call
-  if (lane == 0) {
-    sv[warp] = v;
-    si[warp] = i;
-  }
-  __syncthreads();
-  v = sv[0];
-  i = si[0];
-  for (int w = 1; w < nw; ++w)
-    if (sv[w] > v || (sv[w] == v && si[w] < i)) { v = sv[w]; i = si[w]; }
-}
-
 template <int ACT, int PRO, int EPI>
 __global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
   extern __shared__ __align__(16) float smem[];

@@ -102,6 +102,28 @@ __device__ __forceinline__ float quad_reduce(const float *v, int lane) {
   return m;
 }
 
+// Largest value, lowest index on ties, over the block (all threads return
+// the block's pair; sv, si: one slot per warp).
+__device__ __forceinline__ void block_argmax(float &v, int &i, float *sv, int *si) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();  // the slots may still be read from an earlier call
+  if (lane == 0) {
+    sv[warp] = v;
+    si[warp] = i;
+  }
+  __syncthreads();
+  v = sv[0];
+  i = si[0];
+  for (int w = 1; w < nw; ++w)
+    if (sv[w] > v || (sv[w] == v && si[w] < i)) { v = sv[w]; i = si[w]; }
+}
+
 // Last-block-done: true in exactly one block once every block has published
 // its partials; the counter is left at zero for the next launch.
 __device__ __forceinline__ bool last_block(unsigned *counter) {
@@ -196,7 +218,7 @@ __device__ __forceinline__ void store_xword(int river, int nk, int t, const floa
 // converts and stores, so the L2 round trips of the passes overlap.
 template <int ACT, int PRO>
 __device__ __forceinline__ void stage_x(const GemvArgs &a, const Geo &g, int river, int nk, float r, float *xs) {
-  constexpr int SB = 4;
+  constexpr int SB = 4;  // 8 for the plain vectors measured 1-2% slower (8B decode)
   const int nt = x_words(g, river);
   const float *src = PRO == PRO_NORM ? a.h : a.vec;
   const int nthr = (int)blockDim.x, lane = (int)(threadIdx.x & 31);

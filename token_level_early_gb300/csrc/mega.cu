@@ -407,29 +407,28 @@ __global__ void __launch_bounds__(MW * 32, 1) k_decode_mega(MegaArgs A) {
   {
     PhaseOut po = gemv_run<MW, ACT, PRO_NORM, EPI_LOGITS>(a, 0, xs, scratch, ring, is, bid, nb);
     float *bv = xs;
-    int *bi = reinterpret_cast<int *>(xs + MW * 32);
-    __syncthreads();
-    bv[tid] = po.best;
-    bi[tid] = po.best_i;
-    __syncthreads();
+    int *bi = reinterpret_cast<int *>(xs + MW);
+    float vb = po.best;
+    int ib = po.best_i;
+    block_argmax(vb, ib, bv, bi);
     if (tid == 0) {
-      float vb = bv[0];
-      int ib = bi[0];
-      for (int q = 1; q < MW * 32; ++q)
-        if (bv[q] > vb || (bv[q] == vb && bi[q] < ib)) { vb = bv[q]; ib = bi[q]; }
       head_part[bid * 2] = vb;
       reinterpret_cast<int *>(head_part)[bid * 2 + 1] = ib;
     }
   }
   if (!grid_barrier(A.bar, epoch, A.st.err)) return;
-  if (bid == 0 && tid == 0) {
+  if (bid == 0) {
+    float *bv = xs;
+    int *bi = reinterpret_cast<int *>(xs + MW);
     float vb = -INFINITY;
     int ib = 0x7fffffff;
-    for (int b = 0; b < nb; ++b) {
+    for (int b = tid; b < nb; b += blockDim.x) {
       const float bvv = __ldcg(head_part + b * 2);
       const int bii = __ldcg(reinterpret_cast<const int *>(head_part) + b * 2 + 1);
       if (bvv > vb || (bvv == vb && bii < ib)) { vb = bvv; ib = bii; }
     }
+    block_argmax(vb, ib, bv, bi);
+    if (tid != 0) return;
     A.st.next_ids[0] = ib == 0x7fffffff ? 0 : ib;
     A.st.route[0] = route;
     A.st.exit_layer[0] = exit_l;
