@@ -8,12 +8,19 @@ Llama-3.1-8B-shaped decoder (bf16, river W4A16 group 128), 1024-token random
 prompt, tau = 0.90; the Llama-3.2-1B-shaped workload is reported beside it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload llama8b|llama1b] [--no-cpu-baseline] [--no-secondary]
+                  [--workload llama8b|llama1b|layer8b] [--modes tau,forced,full,river]
+                  [--engine chain|persistent] [--no-cpu-baseline] [--no-secondary]
+                  [--no-fidelity]
 
 value : decode tokens/s, device-timed with CUDA events on the model's stream;
         tokens chained on the device (step i+1 consumes step i's id).
 e2e   : the same metric through rv_decode_step with host buffers (token H2D,
         id + exit layer D2H inside the timed region), wall clock.
+Also in the line: every mode of the decode step (tau rule, forced exits,
+full backbone, all river) with its achieved GB/s, the river vs backbone layer
+time (layer_us), the roofline line of the dominant GEMV, single-kernel
+timings, backbone offloading (layers 1..3 kept), fidelity of the RTN and HQQ
+rivers against the full backbone, the CPU oracle baseline and the 1B shape.
 Multi-GPU: independent replicas (the batch-1 decode step does not shard).
 """
 from __future__ import annotations
