@@ -307,11 +307,19 @@ def cpu_baseline(gm, shape, w, wl, max_seq, tok, tau, log, budget_s=20.0):
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
+    # one more step on a single core (the oracle's results do not depend on
+    # its thread count)
+    one = None
+    if om.set_threads(1) == 0:
+        t1 = time.perf_counter()
+        out = om.decode_step([tok], tau)
+        one = 1.0 / (time.perf_counter() - t1)
     om.close()
-    log(f"[cpu] oracle {n} decode steps in {dt:.1f}s on {nthreads} threads")
+    log(f"[cpu] oracle {n} decode steps in {dt:.1f}s on {nthreads} threads; 1 thread: {one}")
     return {"value": n / dt, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "single_core_value": one,
             "sample": f"{n} oracle decode steps (tau {tau}) of the {shape.name} workload at context "
-                      f"{int(lens[0])}, started from the GPU run's KV cache"}
+                      f"{int(lens[0])}, started from the GPU run's KV cache; one more step on 1 thread"}
 
 
 def kl_div(a, b):

@@ -55,6 +55,7 @@ def lib():
         "ora_free": ([vp], None),
         "ora_quantize_river": ([vp, i32, i32], i32),
         "ora_set_exit_cap": ([vp, i32], i32),
+        "ora_set_threads": ([vp, i32], i32),
         "ora_set_quantizer": ([vp, i32], i32),
         "ora_export_river": ([vp, i32, i32, vp, vp, vp], i32),
         "ora_prefill": ([vp, vp, i32, i32, dbl, i32, vp, vp, vp, vp, vp, vp, vp, vp], i32),
@@ -217,6 +218,13 @@ class Model:
     def set_exit_cap(self, cap: int) -> int:
         """Backbone offloading: keep backbone layers 1..cap; exits are capped at cap."""
         return int(lib().ora_set_exit_cap(self._h, int(cap)))
+
+    def set_threads(self, nthreads: int) -> int:
+        """Host threads for the row loops (results do not depend on it)."""
+        rc = int(lib().ora_set_threads(self._h, int(nthreads)))
+        if rc == RV_OK:
+            self.nthreads = int(nthreads)
+        return rc
 
     def quantize_river(self, group: int, entry_layer: int = 1) -> int:
         rc = lib().ora_quantize_river(self._h, group, entry_layer)

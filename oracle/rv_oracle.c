@@ -666,6 +666,14 @@ int ora_set_exit_cap(ora_model *m, int cap) {
   return RV_OK;
 }
 
+/* Host threads the row loops are split over (1..256); results do not depend
+ * on it (every row's sums run in one thread, in a fixed order). */
+int ora_set_threads(ora_model *m, int nthreads) {
+  if (!m || nthreads < 1 || nthreads > 256) return RV_EINVAL;
+  m->nthreads = nthreads;
+  return RV_OK;
+}
+
 /* River quantizer for the next ora_quantize_river: 0 RTN, 1 HQQ. */
 int ora_set_quantizer(ora_model *m, int method) {
   if (!m || (method != 0 && method != 1)) return RV_EINVAL;

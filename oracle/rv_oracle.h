@@ -48,6 +48,7 @@ int ora_hqq_group(const uint16_t *w, int n, int act, uint8_t *q, uint16_t *s_out
 float ora_hqq_pow_pm1(float a); /* a^(p - 1), p = 0.7, the HQQ shrink's power */
 /* Backbone offloading: keep backbone layers 1..cap; exits are capped at cap. */
 int ora_set_exit_cap(ora_model *m, int cap);
+int ora_set_threads(ora_model *m, int nthreads);
 int ora_prefill(ora_model *m, const int32_t *tokens, int B, int T0, double tau, int fixed_exit,
                 const int32_t *tf_exit, const int32_t *tf_ids, int32_t *next_ids, int32_t *exit_layer,
                 double *dbg_smin, double *dbg_hidden_last, double *dbg_logits, int32_t *n_forced);

@@ -345,3 +345,23 @@ def test_layer_forward_and_head_compose_to_decode_step(tiny_weights):
     assert np.array_equal(logits, ref["logits"]) and np.array_equal(ids, ref["next_ids"])
     assert list(m.lens()) == list(lens)  # positions not advanced
     m.close()
+
+
+def test_thread_count_does_not_change_results():
+    """The oracle's row loops split rows over host threads; every row is
+    computed by one thread in a fixed order, so 1 and 4 threads agree bit
+    for bit (the CPU-baseline timing relies on it)."""
+    shape = synth.TINY
+    w = synth.make_weights(shape)
+    outs = []
+    for nt in (1, 4):
+        m = oracle.Model(shape, w, 2, 24, nthreads=4)
+        assert m.set_threads(nt) == 0
+        assert m.quantize_river(64, 1) == 0
+        p = m.prefill(synth.make_prompt(shape.vocab, 2, 10, seed=9), 0.5, debug=True)
+        d = m.decode_step(p["next_ids"], 0.5, debug=True)
+        outs.append((p["logits"], d["logits"], d["hidden"], d["exit_layer"], m.get_kv()))
+        assert m.set_threads(0) != 0
+        m.close()
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
