@@ -14,8 +14,10 @@
 // thread-block cluster.  Each split streams its share of the past positions
 // 0..p-1 (final before the step starts) through a shared-memory ring that it
 // fills before the programmatic-dependent-launch wait; only q and the K/V of
-// position p come from the QKV kernel it follows.  The splits merge their
-// softmax states through distributed shared memory.
+// position p come from the QKV kernel it follows.  A split whose tiles all
+// fit the ring takes its scores in one pass and one max/sum; longer ones use
+// the online softmax.  The splits merge their softmax states through
+// distributed shared memory.
 #include <cooperative_groups.h>
 #include <math.h>
 

@@ -1,18 +1,22 @@
 // Single-row (batch 1) decode kernels of the River-LLM token-level early exit:
 // one kernel per GEMV of the decode step, launched as a chain.
 //
-//   qkv  : RMSNorm(h) -> [q;k;v] = W_qkv x -> RoPE -> K/V into slot (l, 0, p)
+//   qkv  : exit decision of the layer before (s(l-1) = cos of its input and
+//          output, from the same registers as) RMSNorm(h) -> [q;k;v] = W_qkv x
+//          -> RoPE -> K/V into slot (l, 0, p)
 //   attn : split-KV GQA decode attention (attention.cu)
 //   o    : h_mid = h + W_o o
 //   gu   : RMSNorm(h_mid) -> a = silu(W_g x) * (W_u x)
-//   down : h_out = h_mid + W_d a, s(l) = cos(h, h_out), exit decision
+//   down : h_out = h_mid + W_d a
 // and a final LM-head GEMV with a fused greedy argmax.  Every GEMV reads the
 // row's route flag on the device and streams either the 16-bit backbone
 // matrix or its int4 river copy (same kernel, same grid).  The GEMV itself is
-// the shared core in gemv_core.cuh; here each kernel is one grid over it, its
-// cross-block results combined by the last block to finish.  In a
-// programmatic-dependent-launch chain the kernels other than QKV start their
-// weight streams before waiting on the predecessor.
+// the shared core in gemv_core.cuh; here each kernel is one grid over it (the
+// LM head's blocks combine their argmax candidates in the last block to
+// finish).  In the programmatic-dependent-launch chain every kernel starts
+// its weight stream before waiting on its predecessor; QKV streams the route
+// it reads then and re-streams in the one layer per token where its decision
+// flips the route.
 //
 // Method: "River-LLM: Large Language Model Seamless Exit Based on KV Share",
 // paperlayer.ai summary section 4 (KV-Shared Exit Layer; Inference with
