@@ -423,6 +423,18 @@ def run_reference(wl_name, steps, warmup, budget_s=150.0):
 
 # ------------------------------------------------------------------ main
 
+def slowest_over_ranks(ms, e2e_tokens_per_s, device):
+    """Replicas: the slowest rank's step time and e2e rate (a barrier, then one
+    MAX all-reduce); the whole-job value is world_size tokens per step."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms, 1.0 / e2e_tokens_per_s], dtype=torch.float64, device=device)
+    dist.barrier()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0].item()), 1.0 / float(t[1].item())
+
+
 def layer_us(res, L):
     """River vs backbone layer time (the analogue of the pages' 2.4x): the
     all-river and full-backbone steps minus the LM head's own time, per
@@ -499,11 +511,7 @@ def main():
     ms = tau_r["ms_per_step"]
     e2e = res["e2e_tokens_per_s"]
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, 1.0 / e2e], dtype=torch.float64, device="cuda")
-        dist.barrier()
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e = float(t[0].item()), 1.0 / float(t[1].item())
+        ms, e2e = slowest_over_ranks(ms, e2e, "cuda")
     sec = None
     if not args.no_secondary and world == 1 and args.workload != "layer8b":
         other = "llama1b" if args.workload == "llama8b" else "llama8b"
