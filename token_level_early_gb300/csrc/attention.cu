@@ -156,6 +156,27 @@ static size_t dec_smem(int grp) {
   return (size_t)DNST * DecTile<HD>::BYTES + sizeof(float) * grp * (HD + 2) + sizeof(float) * grp * DNST * DTT;
 }
 
+// q . K[row] for one position: the lane's K row (16-bit, padded) against q as
+// 16-bit pairs, mixed-precision FMAs into four fp32 partial sums.
+template <int HD, int ACT>
+__device__ __forceinline__ float k_dot_q(const unsigned char *krow, const uint32_t *qr) {
+  const uint4 *kr = reinterpret_cast<const uint4 *>(krow);
+  float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < HD / 8; ++j) {
+    const uint4 k = kr[j];
+    d0 = fma_lo16<ACT>(k.x, qr[4 * j], d0);
+    d1 = fma_hi16<ACT>(k.x, qr[4 * j], d1);
+    d2 = fma_lo16<ACT>(k.y, qr[4 * j + 1], d2);
+    d3 = fma_hi16<ACT>(k.y, qr[4 * j + 1], d3);
+    d0 = fma_lo16<ACT>(k.z, qr[4 * j + 2], d0);
+    d1 = fma_hi16<ACT>(k.z, qr[4 * j + 2], d1);
+    d2 = fma_lo16<ACT>(k.w, qr[4 * j + 3], d2);
+    d3 = fma_hi16<ACT>(k.w, qr[4 * j + 3], d3);
+  }
+  return (d0 + d1) + (d2 + d3);
+}
+
 // o[r] += sum over the tile's first n positions t of p[t] * V[t][lane * PER + r],
 // p broadcast from shared memory (all lanes read the same word); full tiles
 // unrolled with two accumulator sets to halve the dependent FMA chains.
@@ -277,23 +298,7 @@ __global__ void __launch_bounds__(GRP * 32, 1) k_attn_dec(AttnArgs a) {
     for (int i = 0; i < DNST - 1; ++i) {
       sc[i] = -INFINITY;
       const int n = i < nt ? min(DTT, p - (tb + i) * DTT) : 0;
-      if (lane < n) {
-        const uint4 *kr = reinterpret_cast<const uint4 *>(sm + i * TL::BYTES + lane * TL::KROW);
-        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-#pragma unroll
-        for (int j = 0; j < PR; ++j) {
-          const uint4 k = kr[j];
-          d0 = fma_lo16<ACT>(k.x, qr[4 * j], d0);
-          d1 = fma_hi16<ACT>(k.x, qr[4 * j], d1);
-          d2 = fma_lo16<ACT>(k.y, qr[4 * j + 1], d2);
-          d3 = fma_hi16<ACT>(k.y, qr[4 * j + 1], d3);
-          d0 = fma_lo16<ACT>(k.z, qr[4 * j + 2], d0);
-          d1 = fma_hi16<ACT>(k.z, qr[4 * j + 2], d1);
-          d2 = fma_lo16<ACT>(k.w, qr[4 * j + 3], d2);
-          d3 = fma_hi16<ACT>(k.w, qr[4 * j + 3], d3);
-        }
-        sc[i] = ((d0 + d1) + (d2 + d3)) * scale;
-      }
+      if (lane < n) sc[i] = k_dot_q<HD, ACT>(sm + i * TL::BYTES + lane * TL::KROW, qr) * scale;
       mx = fmaxf(mx, sc[i]);
     }
     mx = warp_max(mx);
@@ -322,23 +327,7 @@ __global__ void __launch_bounds__(GRP * 32, 1) k_attn_dec(AttnArgs a) {
       const unsigned char *tv = tk + DTT * TL::KROW;
       const int n = min(DTT, p - tile * DTT);
       float sc = -INFINITY;
-      if (lane < n) {
-        const uint4 *kr = reinterpret_cast<const uint4 *>(tk + lane * TL::KROW);
-        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-#pragma unroll
-        for (int j = 0; j < PR; ++j) {
-          const uint4 k = kr[j];
-          d0 = fma_lo16<ACT>(k.x, qr[4 * j], d0);
-          d1 = fma_hi16<ACT>(k.x, qr[4 * j], d1);
-          d2 = fma_lo16<ACT>(k.y, qr[4 * j + 1], d2);
-          d3 = fma_hi16<ACT>(k.y, qr[4 * j + 1], d3);
-          d0 = fma_lo16<ACT>(k.z, qr[4 * j + 2], d0);
-          d1 = fma_hi16<ACT>(k.z, qr[4 * j + 2], d1);
-          d2 = fma_lo16<ACT>(k.w, qr[4 * j + 3], d2);
-          d3 = fma_hi16<ACT>(k.w, qr[4 * j + 3], d3);
-        }
-        sc = ((d0 + d1) + (d2 + d3)) * scale;
-      }
+      if (lane < n) sc = k_dot_q<HD, ACT>(tk + lane * TL::KROW, qr) * scale;
       const float mnew = fmaxf(mrun, warp_max(sc));
       const float pe = lane < n ? expf(sc - mnew) : 0.f;
       const float corr = mrun == -INFINITY ? 0.f : expf(mrun - mnew);
