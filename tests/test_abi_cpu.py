@@ -34,3 +34,27 @@ def test_error_paths_without_gpu_work():
     assert lib.rv_load_model(None, None, None, None) == rv.RV_EINVAL
     assert lib.rv_kv_bytes(None) == 0
     lib.rv_free_model(None)
+
+
+def test_every_entry_point_rejects_a_null_handle():
+    """Each call checks its handle and pointers before any CUDA work, so these
+    run on a machine without a GPU and return RV_EINVAL (or 0 / a message)."""
+    import ctypes as C
+
+    lib = rv.lib()
+    E = rv.RV_EINVAL
+    buf = (C.c_int32 * 4)()
+    assert lib.rv_prefill(None, buf, 1, 1, C.c_float(0.9), -1, buf, buf) == E
+    assert lib.rv_decode_step_dev(None, buf, 1, C.c_float(0.9), None, buf, buf, None) == E
+    assert lib.rv_sync_status(None) == E
+    assert lib.rv_kv_reset(None, None, 0) == E
+    assert lib.rv_set_debug(None, 1) == E
+    assert lib.rv_set_option(None, rv.OPT_QUANTIZER, rv.QUANT_HQQ) == E
+    assert lib.rv_debug_dump(None, rv.DUMP_LOGITS, buf, 16) == E
+    assert lib.rv_export_river(None, 1, 0, buf, buf, buf) == E
+    assert lib.rv_offload_backbone(None, 1) == E
+    assert lib.rv_param_bytes(None, 0) == 0
+    ms, by = C.c_float(0), C.c_double(0)
+    assert lib.rv_time_kernel(None, rv.TIME_GATEUP, 1, 0, 1, C.byref(ms), C.byref(by)) == E
+    assert lib.rv_greedy_head_noalloc(None, None, None, 8, 8, 1, C.c_float(1e-5), None, None, None) == E
+    assert b"null" in lib.rv_last_error()
