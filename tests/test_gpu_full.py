@@ -40,11 +40,12 @@ def check_prefill_last_position(gm, om, prompt, g_next, g_exit, act):
             assert rel_l2(a, r) <= 3e-2
 
 
-def run_single(name, sample_steps, mode):
+def run_single(name, sample_steps, mode, tau=None, engine=rv.ENGINE_CHAIN, steps=None):
     wl = synth.WORKLOADS[name]
     shape = wl.shape
     w = synth.make_weights(shape)
-    T = wl.prompt_len + wl.steps
+    n_steps = wl.steps if steps is None else steps
+    T = wl.prompt_len + n_steps
     gm = rv.Model(shape, w, 1, T)
     om = oracle.Model(shape, w, 1, T)
     gm.quantize_river(wl.group, 1)
@@ -57,6 +58,7 @@ def run_single(name, sample_steps, mode):
             for a, b in zip(g, o):
                 assert np.array_equal(a, b), (layer, proj)
     gm.set_debug(True)
+    gm.set_engine(engine)
     prompt = synth.make_prompt(shape.vocab, 1, wl.prompt_len)
     g_next, g_exit = gm.prefill(prompt, wl.prefill_tau)
     s_min = gm.dump(rv.DUMP_S)[:, 0]
@@ -64,14 +66,14 @@ def run_single(name, sample_steps, mode):
     exp = next((l for l in range(1, shape.n_layers) if s_min[l - 1] > wl.prefill_tau), shape.n_layers)
     assert g_exit[0] == exp, (g_exit, s_min)
     check_prefill_last_position(gm, om, prompt, g_next, g_exit, shape.act_dtype)
-    tau = wl.taus[0]
+    tau = wl.taus[0] if tau is None else tau
     tok = [int(g_next[0])]
     exits = []
-    for step in range(wl.steps):
+    for step in range(n_steps):
         forced = synth.forced_exits(step, 1, shape.n_layers) if mode == "forced" else None
         if step in sample_steps:
             nxt, ex = sampled_step(gm, om, tok, tau, forced, 1, shape.n_layers, shape.act_dtype, 1,
-                                   f"{name}:{mode}:{step}")
+                                   f"{name}:{mode}:{tau}:{engine}:{step}")
         else:
             nxt, ex = gm.decode_step(tok, tau, forced)
         if forced is not None:
@@ -87,8 +89,10 @@ def run_single(name, sample_steps, mode):
     return exits
 
 
-def test_llama1b_tau_rule_workload():
-    exits = run_single("llama1b", {0, 1, 2, 17, 128, 255}, "tau")
+@pytest.mark.parametrize("tau", synth.WORKLOADS["llama1b"].taus)
+def test_llama1b_tau_rule_workload(tau):
+    """The 1B workload's tau sweep: 0.85, 0.90 and 0.95."""
+    exits = run_single("llama1b", {0, 1, 2, 17, 128, 255}, "tau", tau)
     assert len(exits) == 256
 
 
@@ -138,3 +142,25 @@ def test_batch64_mixed_exits():
     assert not (kv[:, :, :B, :, :T] == 0x7FFF).any()
     gm.close()
     om.close()
+
+
+# The persistent decode engine (one cooperative launch per step, weights
+# streamed through a shared-memory ring by a producer warp) on the same
+# workloads, checked against the oracle the same way.
+
+def test_stream_llama1b_tau_rule_workload():
+    exits = run_single("llama1b", {0, 1, 2, 100, 255}, "tau", 0.90, rv.ENGINE_PERSISTENT)
+    assert len(exits) == 256
+
+
+def test_stream_llama1b_forced_exit_workload():
+    exits = run_single("llama1b", {0, 3, 64}, "forced", None, rv.ENGINE_PERSISTENT, steps=128)
+    assert min(exits) >= 1
+
+
+def test_stream_llama8b_tau_rule_workload():
+    run_single("llama8b", {0, 1, 100, 511}, "tau", None, rv.ENGINE_PERSISTENT)
+
+
+def test_stream_llama8b_forced_exit_workload():
+    run_single("llama8b", {0, 5, 300}, "forced", None, rv.ENGINE_PERSISTENT, steps=320)

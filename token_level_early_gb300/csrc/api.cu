@@ -21,7 +21,7 @@
 #include "common.cuh"
 #include "gemv_core.cuh"
 #include "kernels.cuh"
-#include "mega.cuh"
+#include "stream.cuh"
 
 using namespace rv;
 
@@ -54,7 +54,7 @@ enum { MAT_QKV = 0, MAT_O = 1, MAT_GU = 2, MAT_D = 3, N_MAT = 4 };
 struct RiverDev {
   uint32_t *q = nullptr;
   __half2 *sz = nullptr;
-  int Kp = 0, G = 0;
+  int Kp = 0, G = 0, Gs = 0;  // Gs: row stride of sz (G padded to a multiple of 4)
 };
 
 struct LayerDev {
@@ -123,13 +123,13 @@ struct rv_model {
   // graphs
   std::map<int, cudaGraphExec_t> graphs;
 
-  // persistent batch-1 step
+  // persistent batch-1 step (stream.cu)
   int engine = RV_ENGINE_CHAIN;
-  bool mega_ready = false;
-  int mega_grid = 0;
+  bool stream_ready = false;
+  int stream_grid = 0;
   LayerDesc *d_layers = nullptr;
   unsigned *bar = nullptr;
-  MegaArgs mega{};
+  StreamArgs sargs{};
 };
 
 namespace {
@@ -207,6 +207,7 @@ Mat make_mat(const rv_model *m, const LayerDev &ly, int which) {
     mt.r.sz = ly.r[which].sz;
     mt.r.Kp = ly.r[which].Kp;
     mt.r.G = ly.r[which].G;
+    mt.r.Gs = ly.r[which].Gs;
     mt.r.g = m->group;
   }
   return mt;
@@ -432,29 +433,33 @@ int enqueue_step_rows(rv_model *m, int B, cudaStream_t s) {
 }
 
 // (Re)build the persistent kernel's argument block: layer descriptors (with
-// the river copies when built), activations, scratch, debug pointers.
-int build_mega(rv_model *m) {
-  m->mega_ready = false;
+// the river copies when built), activations, scratch, debug pointers, and the
+// size of its activation region (the largest staged vector of any phase, or
+// the attention's K/V tiles).
+int build_stream(rv_model *m) {
+  m->stream_ready = false;
+  const int grp = m->H / m->Hkv;
+  if (!stream_supported(m->hd, grp, m->act, m->has_river ? m->group : 0)) return RV_OK;
   std::vector<LayerDesc> h(m->L);
-  size_t xs = 0;
+  int xb = 0;
   for (int l = 0; l < m->L; ++l) {
     for (int i = 0; i < N_MAT; ++i) {
       h[l].m[i] = make_mat(m, m->layers[l], i);
-      const size_t f = x_floats(geo_of(h[l].m[i]));
-      if (f > xs) xs = f;
+      if (h[l].m[i].w) xb = std::max(xb, x_geom(h[l].m[i], 0).bytes);
+      if (m->has_river) xb = std::max(xb, x_geom(h[l].m[i], 1).bytes);
     }
     h[l].attn_norm = m->layers[l].attn_norm;
     h[l].mlp_norm = m->layers[l].mlp_norm;
   }
   Mat lm{};
   lm.w = m->lm_head; lm.N = m->V; lm.K = m->d;
-  if (x_floats(geo_of(lm)) > xs) xs = x_floats(geo_of(lm));
-  const size_t at = mega_attn_tile_floats(m->hd, m->H / m->Hkv);
-  if (at > xs) xs = at;
-  if ((size_t)mega_warps() * 32 * 2 > xs) xs = (size_t)mega_warps() * 32 * 2;  // head argmax scratch
+  xb = std::max(xb, x_geom(lm, 0).bytes);
+  // attention: two K/V tiles of 32 positions (K rows padded by 16 bytes) + q of a group as 16-bit
+  xb = std::max(xb, 2 * sk::ATILE * (m->hd * 2 + 16 + m->hd * 2) + grp * m->hd * 2);
+  xb = (xb + 127) & ~127;
   RV_CK(cudaMemcpy(m->d_layers, h.data(), sizeof(LayerDesc) * m->L, cudaMemcpyHostToDevice));
-  MegaArgs &A = m->mega;
-  A = MegaArgs{};
+  StreamArgs &A = m->sargs;
+  A = StreamArgs{};
   A.layers = m->d_layers;
   A.embed = m->embed; A.final_norm = m->final_norm; A.lm_head = m->lm_head;
   A.L = m->L; A.d = m->d; A.H = m->H; A.Hkv = m->Hkv; A.hd = m->hd; A.F = m->F; A.V = m->V; A.act = m->act;
@@ -465,33 +470,35 @@ int build_mega(rv_model *m) {
   A.st = m->st;
   A.h[0] = m->hbuf[0]; A.h[1] = m->hbuf[1]; A.hmid = m->hmid; A.q = m->qbuf; A.o = m->obuf; A.a = m->abuf;
   A.attn_part = m->attn_part;
+  A.attn_counter = m->attn_counter;
   int sp = m->n_sm / m->Hkv;
   if (sp > m->attn_splits_max) sp = m->attn_splits_max;
-  A.splits = sp < 1 ? 1 : sp;
+  A.att_splits = sp < 1 ? 1 : sp;
   A.partials = m->partials;
   A.bar = m->bar;
   A.dbg_h = m->debug ? m->dbg_h : nullptr;
   A.dbg_s = m->debug ? m->dbg_s : nullptr;
   A.dbg_logits = m->debug ? m->dbg_logits : nullptr;
-  A.xs_floats = (xs + 3) & ~(size_t)3;
+  A.xbytes = xb;
+  A.nstages = 0;  // set by stream_prepare from the device's shared memory
   int grid = 0;
-  cudaError_t e = mega_prepare(A, m->n_sm, &grid);
+  cudaError_t e = stream_prepare(A, m->n_sm, &grid);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return RV_OK;  // not resident on this device: the kernel chain serves
   }
-  m->mega_grid = grid;
-  m->mega_ready = true;
+  m->stream_grid = grid;
+  m->stream_ready = true;
   return RV_OK;
 }
 
 // Launch one decode step (persistent kernel for batch 1 when selected, else
 // the captured graph for batch B, captured once per batch size).
 int launch_step(rv_model *m, int B) {
-  if (B == 1 && m->engine == RV_ENGINE_PERSISTENT && m->mega_ready) {
+  if (B == 1 && m->engine == RV_ENGINE_PERSISTENT && m->stream_ready) {
     RV_CK(cudaMemsetAsync(m->st.err, 0, sizeof(int32_t), m->stream));
     RV_CK(cudaMemsetAsync(m->bar, 0, sizeof(unsigned) * 2, m->stream));  // fresh barrier every step
-    RV_CK(mega_launch(m->mega, m->mega_grid, m->stream));
+    RV_CK(stream_launch(m->sargs, m->stream_grid, m->stream));
     return RV_OK;
   }
   auto it = m->graphs.find(B);
@@ -677,7 +684,7 @@ static int load_impl(rv_model *m, const rv_config *cfg, const void *const *weigh
   RV_ALLOC(A, m->bar, sizeof(unsigned) * 2);
   RV_CK(cudaMemsetAsync(m->bar, 0, sizeof(unsigned) * 2, m->stream));
   RV_CK(cudaStreamSynchronize(m->stream));
-  return build_mega(m);
+  return build_stream(m);
 }
 
 int rv_load_model(const rv_config *cfg, const void *const *weights, void *stream, rv_model **out) {
@@ -727,7 +734,7 @@ int rv_quantize_river(rv_model *m, int group_size, int entry_layer) {
   drop_graphs(m);
   free_list(m->river_allocs);
   m->has_river = false;
-  m->mega_ready = false;
+  m->stream_ready = false;
   m->group = group_size;
   for (LayerDev &ly : m->layers)
     for (int i = 0; i < N_MAT; ++i) ly.r[i] = RiverDev{};
@@ -738,9 +745,11 @@ int rv_quantize_river(rv_model *m, int group_size, int entry_layer) {
       RiverDev &r = ly.r[i];
       r.Kp = round32(mt.K);
       r.G = (mt.K + group_size - 1) / group_size;
+      r.Gs = pad_groups(r.G);
       auto &A = m->river_allocs;
       RV_ALLOC(A, r.q, sizeof(uint32_t) * (size_t)mt.N * (r.Kp / 8));
-      RV_ALLOC(A, r.sz, sizeof(__half2) * (size_t)mt.N * r.G);
+      RV_ALLOC(A, r.sz, sizeof(__half2) * (size_t)mt.N * r.Gs);
+      if (r.Gs != r.G) RV_CK(cudaMemsetAsync(r.sz, 0, sizeof(__half2) * (size_t)mt.N * r.Gs, m->stream));
       if (m->quantizer == RV_QUANT_HQQ)
         RV_CK(launch_hqq_quantize(mt.w, mt.N, mt.K, m->act, group_size, r.Kp, r.q, r.sz, m->st.err, m->stream));
       else
@@ -752,12 +761,12 @@ int rv_quantize_river(rv_model *m, int group_size, int entry_layer) {
   RV_CK(cudaStreamSynchronize(m->stream));
   if (err & 4) {
     free_list(m->river_allocs);
-    build_mega(m);
+    build_stream(m);
     return fail(RV_EINVAL, "a group's scale overflows fp16");
   }
   m->has_river = true;
   m->entry = entry_layer;
-  return build_mega(m);
+  return build_stream(m);
 }
 
 int rv_export_river(const rv_model *m, int layer, int proj, void *q_packed, void *scales, void *zeros) {
@@ -779,13 +788,19 @@ int rv_export_river(const rv_model *m, int layer, int proj, void *q_packed, void
   if (q_packed)
     RV_CK(cudaMemcpy2D(q_packed, sizeof(uint32_t) * (K / 8), r.q + (size_t)row0 * (r.Kp / 8), sizeof(uint32_t) * (r.Kp / 8),
                        sizeof(uint32_t) * (K / 8), rows, cudaMemcpyDeviceToHost));
-  // (scale, zero) pairs are interleaved on the device: pick each half with a pitched copy
-  const __half *sz0 = reinterpret_cast<const __half *>(r.sz + (size_t)row0 * r.G);
-  const size_t n_sz = (size_t)rows * r.G;
-  if (scales)
-    RV_CK(cudaMemcpy2D(scales, sizeof(__half), sz0, sizeof(__half2), sizeof(__half), n_sz, cudaMemcpyDeviceToHost));
-  if (zeros)
-    RV_CK(cudaMemcpy2D(zeros, sizeof(__half), sz0 + 1, sizeof(__half2), sizeof(__half), n_sz, cudaMemcpyDeviceToHost));
+  // (scale, zero) pairs are interleaved on the device in rows padded to Gs
+  // pairs: copy the rows, then pick each half on the host
+  if (scales || zeros) {
+    std::vector<__half2> tmp((size_t)rows * r.Gs);
+    RV_CK(cudaMemcpy(tmp.data(), r.sz + (size_t)row0 * r.Gs, sizeof(__half2) * tmp.size(), cudaMemcpyDeviceToHost));
+    uint16_t *so = static_cast<uint16_t *>(scales), *zo = static_cast<uint16_t *>(zeros);
+    for (int n = 0; n < rows; ++n)
+      for (int gi = 0; gi < r.G; ++gi) {
+        const __half2 v = tmp[(size_t)n * r.Gs + gi];
+        if (so) so[(size_t)n * r.G + gi] = __half_as_ushort(__low2half(v));
+        if (zo) zo[(size_t)n * r.G + gi] = __half_as_ushort(__high2half(v));
+      }
+  }
   return RV_OK;
 }
 
@@ -803,12 +818,14 @@ static int validate_step(rv_model *m, int B, const int32_t *forced_host, bool fo
   return RV_OK;
 }
 
-// Device error flags -> status: bit 3 = a persistent-kernel grid barrier
-// gave up waiting, bit 4 = a tensor-core GEMM wait gave up; the other bits
-// flag invalid inputs (token, forced exit, quantization).
+// Device error flags -> status: 8 = a persistent-kernel grid barrier gave up
+// waiting, 16 = a tensor-core GEMM wait gave up, 32 = a persistent-kernel
+// stage or route wait gave up; the other bits flag invalid inputs (token,
+// forced exit, quantization).
 static int device_status(int32_t err) {
   if (err & 8) return fail(RV_ETIMEOUT, "a grid barrier of the persistent decode kernel timed out (0x%x)", err);
   if (err & 16) return fail(RV_ETIMEOUT, "a bounded wait of the tensor-core GEMM gave up (0x%x)", err);
+  if (err & 32) return fail(RV_ETIMEOUT, "a bounded wait of the persistent decode kernel's weight ring gave up (0x%x)", err);
   return fail(RV_EINVAL, "device flagged an invalid input (0x%x)", err);
 }
 
@@ -967,7 +984,7 @@ int rv_set_debug(rv_model *m, int enable) {
   }
   if ((bool)enable != m->debug) drop_graphs(m);
   m->debug = enable != 0;
-  return build_mega(m);
+  return build_stream(m);
 }
 
 int rv_set_option(rv_model *m, int option, int value) {
@@ -980,7 +997,7 @@ int rv_set_option(rv_model *m, int option, int value) {
   }
   if (option != RV_OPT_DECODE_ENGINE) return fail(RV_EINVAL, "unknown option %d", option);
   if (value != RV_ENGINE_CHAIN && value != RV_ENGINE_PERSISTENT) return fail(RV_EINVAL, "unknown engine %d", value);
-  if (value == RV_ENGINE_PERSISTENT && !m->mega_ready)
+  if (value == RV_ENGINE_PERSISTENT && !m->stream_ready)
     return fail(RV_ESTATE, "the persistent decode kernel cannot be made resident on this device");
   RV_CK(cudaStreamSynchronize(m->stream));
   m->engine = value;
@@ -1098,7 +1115,7 @@ int rv_offload_backbone(rv_model *m, int keep_layers) {
   const int32_t cap = keep_layers;
   RV_CK(cudaMemcpy(const_cast<int32_t *>(m->st.cap), &cap, sizeof(int32_t), cudaMemcpyHostToDevice));
   m->cap = keep_layers;
-  return build_mega(m);
+  return build_stream(m);
 }
 
 size_t rv_param_bytes(const rv_model *m, int which) {

@@ -106,12 +106,14 @@ __device__ __forceinline__ float3 block_sum3(float a, float b, float c, float *s
 
 // River copy of one projection in the device layout: canonical packing with
 // the row stride padded to Kp (a multiple of 32) nibbles; fp16 scale and zero
-// per (row, group of g columns), interleaved as one half2 (scale, zero).
+// per (row, group of g columns), interleaved as one half2 (scale, zero), each
+// row of groups padded to Gs = a multiple of 4 (16 bytes) with zero pairs.
 struct RiverMat {
   const uint32_t *q;   // [N][Kp/8]
-  const __half2 *sz;   // [N][G]
-  int Kp, G, g;
+  const __half2 *sz;   // [N][Gs]
+  int Kp, G, g, Gs;
 };
+__host__ __device__ __forceinline__ int pad_groups(int G) { return (G + 3) & ~3; }
 
 // One projection: backbone 16-bit matrix [N][K] and its river copy.
 struct Mat {

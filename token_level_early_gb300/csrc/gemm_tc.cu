@@ -226,7 +226,7 @@ __global__ void k_river_split(RiverMat r, int N, int K, int act, uint16_t *hi, u
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
     const int n = (int)(i / (K / 8)), k0 = (int)(i - (long)n * (K / 8)) * 8;
     const uint32_t word = r.q[(size_t)n * words + (k0 >> 3)];
-    const float2 sz = __half22float2(r.sz[(size_t)n * r.G + k0 / r.g]);
+    const float2 sz = __half22float2(r.sz[(size_t)n * r.Gs + k0 / r.g]);
     uint16_t h[8], l[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {

@@ -141,11 +141,12 @@ __device__ __forceinline__ bool last_block(unsigned *counter) {
 }
 
 struct Geo {
-  int K, Kp, nk4, nk16, words, G;
+  int K, Kp, nk4, nk16, words, G, Gs;
   int gpc;  // groups per int4 chunk when the group size divides the chunk, else 0
   int spr;  // 16-byte pieces of one row's (scale, zero) words per chunk, when
-            // they can be copied as such (gpc a multiple of 4, rows 16-byte
-            // aligned); else 0 and every lane copies its own group's word
+            // they can be copied as such (gpc a multiple of 4; rows of groups
+            // are padded to 16 bytes); else 0 and every lane copies its own
+            // group's word
 };
 
 __host__ __device__ __forceinline__ Geo geo_of(const Mat &m) {
@@ -156,8 +157,9 @@ __host__ __device__ __forceinline__ Geo geo_of(const Mat &m) {
   g.nk16 = (m.K + CH16 - 1) / CH16;
   g.words = g.Kp >> 3;
   g.G = m.r.G;
+  g.Gs = m.r.Gs;
   g.gpc = (m.r.g > 0 && CH4 % m.r.g == 0) ? CH4 / m.r.g : 0;
-  g.spr = (g.gpc >= 4 && g.gpc % 4 == 0 && g.G % 4 == 0) ? g.gpc / 4 : 0;
+  g.spr = (g.gpc >= 4 && g.gpc % 4 == 0) ? g.gpc / 4 : 0;
   return g;
 }
 
@@ -345,8 +347,8 @@ __device__ __forceinline__ void stream_rows(const GemvArgs &a, const Geo &g, int
   const uint32_t stride = (uint32_t)(river ? g.words : g.K);
   is.off0 = (uint32_t)rows[0] * stride;
   is.off2 = (uint32_t)rows[2] * stride;
-  is.soff0 = (uint32_t)rows[0] * (uint32_t)g.G;
-  is.soff2 = (uint32_t)rows[2] * (uint32_t)g.G;
+  is.soff0 = (uint32_t)rows[0] * (uint32_t)g.Gs;
+  is.soff2 = (uint32_t)rows[2] * (uint32_t)g.Gs;
 }
 
 // Copy the next item of the stream into `stage` (one commit group per call,
@@ -370,16 +372,16 @@ __device__ __forceinline__ void issue_item(const GemvArgs &a, const Geo &g, int 
           const unsigned ss = (unsigned)__cvta_generic_to_shared(stage) + STAGE_W + lane * 4;
           const __half2 *s0 = sb + is.soff0, *s2 = sb + is.soff2;
           cp4s(ss, s0);
-          cp4s(ss + 128, s0 + g.G);
+          cp4s(ss + 128, s0 + g.Gs);
           cp4s(ss + 256, s2);
-          cp4s(ss + 384, s2 + g.G);
+          cp4s(ss + 384, s2 + g.Gs);
         }
       }
       if (g.spr && lane < 4 * g.spr) {  // the chunk's groups of the 4 rows: row r at r * gpc
         const int r = lane / g.spr, piece = lane - r * g.spr;
         if (is.c * g.gpc + piece * 4 < g.G)  // a ragged last chunk has fewer groups
           cp16s((unsigned)__cvta_generic_to_shared(stage) + STAGE_W + (r * g.gpc + piece * 4) * 4,
-                a.m.r.sz + (r < 2 ? is.soff0 : is.soff2) + (r & 1) * g.G + is.c * g.gpc + piece * 4);
+                a.m.r.sz + (r < 2 ? is.soff0 : is.soff2) + (r & 1) * g.Gs + is.c * g.gpc + piece * 4);
       }
     } else {
       const int k0 = is.c * CH16 + lane * 8;

@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(256) k_gemm_rows(Mat mt, int river, int act, c
           const RiverMat &R = mt.r;
           const uint32_t word = R.q[(size_t)n * (R.Kp >> 3) + (k >> 3)];
           const int gi = k / R.g;
-          const float2 szf = __half22float2(R.sz[(size_t)n * R.G + gi]);
+          const float2 szf = __half22float2(R.sz[(size_t)n * R.Gs + gi]);
           const float s = szf.x, z = szf.y;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {

@@ -10,7 +10,8 @@
 //   q = clamp(rint(w / s) + z, 0, 15)  (rint: half to even)
 // Codes are packed 8 per uint32, element k of a row in bits 4*(k%8) of word
 // k/8, each row padded to Kp (a multiple of 32) with zero codes; scale and
-// zero of a group are stored side by side as one half2.
+// zero of a group are stored side by side as one half2, rows of groups
+// padded to a multiple of 4 pairs (left as the allocation's zeros).
 #include <math.h>
 
 #include "common.cuh"
@@ -20,7 +21,7 @@ namespace rv {
 
 __global__ void k_rtn(const uint16_t *W, int N, int K, int act, int g, int Kp, uint32_t *q, __half2 *sz,
                       int32_t *err) {
-  const int G = (K + g - 1) / g, words = Kp >> 3;
+  const int G = (K + g - 1) / g, Gs = pad_groups(G), words = Kp >> 3;
   const long total = (long)N * G;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
     const int n = (int)(i / G), gi = (int)(i % G);
@@ -59,7 +60,7 @@ __global__ void k_rtn(const uint16_t *W, int N, int K, int act, int g, int Kp, u
       }
       q[(size_t)n * words + (kb >> 3)] = word;
     }
-    sz[(size_t)n * G + gi] = __halves2half2(s16, __float2half_rn(z));
+    sz[(size_t)n * Gs + gi] = __halves2half2(s16, __float2half_rn(z));
   }
 }
 
@@ -111,7 +112,7 @@ __device__ __forceinline__ float hqq_pow_pm1(float a) {  // a^(p - 1), p = 0.7, 
 __device__ __forceinline__ float clamp15(float r) { return r < 0.0f ? 0.0f : (r > 15.0f ? 15.0f : r); }
 
 __global__ void k_hqq(const uint16_t *W, int N, int K, int act, int g, int Kp, uint32_t *q, __half2 *sz, int32_t *err) {
-  const int G = (K + g - 1) / g, words = Kp >> 3;
+  const int G = (K + g - 1) / g, Gs = pad_groups(G), words = Kp >> 3;
   const long total = (long)N * G;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
     const int n = (int)(i / G), gi = (int)(i % G);
@@ -160,9 +161,9 @@ __global__ void k_hqq(const uint16_t *W, int N, int K, int act, int g, int Kp, u
       }
       const __half z16 = __float2half_rn(z);
       zq = __half2float(z16);
-      sz[(size_t)n * G + gi] = __halves2half2(s16, z16);
+      sz[(size_t)n * Gs + gi] = __halves2half2(s16, z16);
     } else {
-      sz[(size_t)n * G + gi] = __halves2half2(s16, __float2half_rn(0.0f));
+      sz[(size_t)n * Gs + gi] = __halves2half2(s16, __float2half_rn(0.0f));
     }
     for (int kb = k0; kb < k0 + g && kb < Kp; kb += 8) {
       uint32_t word = 0;
