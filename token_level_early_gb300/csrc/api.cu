@@ -128,6 +128,7 @@ struct rv_model {
   bool stream_ready = false;
   int stream_grid = 0;
   LayerDesc *d_layers = nullptr;
+  CUtensorMap *d_tmaps = nullptr;  // [12 L + 1]: per layer and matrix the 16-bit, code and scale maps; LM head
   unsigned *bar = nullptr;
   StreamArgs sargs{};
 };
@@ -151,6 +152,18 @@ int dalloc(rv_model *m, std::vector<void *> &list, void **p, size_t bytes) {
   do {                                                                          \
     int rc_ = dalloc(m, list, reinterpret_cast<void **>(&(ptr)), (bytes));      \
     if (rc_ != RV_OK) return rc_;                                               \
+  } while (0)
+
+// Weight matrices get kWeightPad zeroed bytes past their end: the persistent
+// engine's tensor copies move whole boxes, and a row's last box may run past
+// the row (and, for the last row, past the matrix) when K is not a multiple
+// of the box; the extra values only ever meet zero activations.
+constexpr size_t kWeightPad = 256;
+#define RV_ALLOC_W(list, ptr, bytes)                                                               \
+  do {                                                                                             \
+    const size_t b_ = (bytes);                                                                     \
+    RV_ALLOC(list, ptr, b_ + kWeightPad);                                                          \
+    RV_CK(cudaMemsetAsync(reinterpret_cast<char *>(ptr) + b_, 0, kWeightPad, m->stream));           \
   } while (0)
 
 void free_list(std::vector<void *> &list) {
@@ -441,27 +454,45 @@ int build_stream(rv_model *m) {
   const int grp = m->H / m->Hkv;
   if (!stream_supported(m->hd, grp, m->act, m->has_river ? m->group : 0)) return RV_OK;
   std::vector<LayerDesc> h(m->L);
+  std::vector<CUtensorMap> tm(12 * (size_t)m->L + 1);
   int xb = 0;
   for (int l = 0; l < m->L; ++l) {
     for (int i = 0; i < N_MAT; ++i) {
-      h[l].m[i] = make_mat(m, m->layers[l], i);
-      if (h[l].m[i].w) xb = std::max(xb, x_geom(h[l].m[i], 0).bytes);
-      if (m->has_river) xb = std::max(xb, x_geom(h[l].m[i], 1).bytes);
+      const Mat mt = make_mat(m, m->layers[l], i);
+      h[l].m[i] = mt;
+      CUtensorMap *t = &tm[(size_t)12 * l + 3 * i];
+      const CUtensorMap *dt = m->d_tmaps + (size_t)12 * l + 3 * i;
+      h[l].tw[i] = h[l].tq[i] = h[l].ts[i] = nullptr;
+      if (mt.w) {
+        if (!stream_map_w16(&t[0], mt.w, mt.N, mt.K, m->act)) return RV_OK;  // no tensor maps: the chain serves
+        h[l].tw[i] = dt;
+        xb = std::max(xb, x_geom(mt, 0).bytes);
+      }
+      if (m->has_river) {
+        if (!stream_map_q(&t[1], mt.r.q, mt.N, mt.r.Kp) || !stream_map_sz(&t[2], mt.r.sz, mt.N, mt.r.Gs, mt.r.g))
+          return RV_OK;
+        h[l].tq[i] = dt + 1;
+        h[l].ts[i] = dt + 2;
+        xb = std::max(xb, x_geom(mt, 1).bytes);
+      }
     }
     h[l].attn_norm = m->layers[l].attn_norm;
     h[l].mlp_norm = m->layers[l].mlp_norm;
   }
   Mat lm{};
   lm.w = m->lm_head; lm.N = m->V; lm.K = m->d;
+  if (!stream_map_w16(&tm[(size_t)12 * m->L], lm.w, lm.N, lm.K, m->act)) return RV_OK;
   xb = std::max(xb, x_geom(lm, 0).bytes);
   // attention: two K/V tiles of 32 positions (K rows padded by 16 bytes) + q of a group as 16-bit
   xb = std::max(xb, 2 * sk::ATILE * (m->hd * 2 + 16 + m->hd * 2) + grp * m->hd * 2);
   xb = (xb + 127) & ~127;
   RV_CK(cudaMemcpy(m->d_layers, h.data(), sizeof(LayerDesc) * m->L, cudaMemcpyHostToDevice));
+  RV_CK(cudaMemcpy(m->d_tmaps, tm.data(), sizeof(CUtensorMap) * tm.size(), cudaMemcpyHostToDevice));
   StreamArgs &A = m->sargs;
   A = StreamArgs{};
   A.layers = m->d_layers;
   A.embed = m->embed; A.final_norm = m->final_norm; A.lm_head = m->lm_head;
+  A.t_head = m->d_tmaps + (size_t)12 * m->L;
   A.L = m->L; A.d = m->d; A.H = m->H; A.Hkv = m->Hkv; A.hd = m->hd; A.F = m->F; A.V = m->V; A.act = m->act;
   A.Bmax = m->Bmax;
   A.eps = m->c.rms_eps;
@@ -595,14 +626,14 @@ static int load_impl(rv_model *m, const rv_config *cfg, const void *const *weigh
     int rc_ = up((dst), (src), (n)); \
     if (rc_) return rc_;             \
   } while (0)
-  RV_ALLOC(A, m->embed, e2 * V * d);
+  RV_ALLOC_W(A, m->embed, e2 * V * d);
   RV_UP(m->embed, weights[0], (size_t)V * d);
   RV_ALLOC(A, m->final_norm, e2 * d);
   RV_UP(m->final_norm, weights[1], d);
   if (c.tied_embed) {
     m->lm_head = m->embed;
   } else {
-    RV_ALLOC(A, m->lm_head, e2 * V * d);
+    RV_ALLOC_W(A, m->lm_head, e2 * V * d);
     RV_UP(m->lm_head, weights[2], (size_t)V * d);
   }
   m->layers.resize(m->L);
@@ -613,16 +644,16 @@ static int load_impl(rv_model *m, const rv_config *cfg, const void *const *weigh
     RV_UP(ly.attn_norm, w[0], d);
     RV_ALLOC(A, ly.mlp_norm, e2 * d);
     RV_UP(ly.mlp_norm, w[5], d);
-    RV_ALLOC(A, ly.w[MAT_QKV], e2 * m->qkv_n * d);
+    RV_ALLOC_W(A, ly.w[MAT_QKV], e2 * m->qkv_n * d);
     RV_UP(ly.w[MAT_QKV], w[1], (size_t)m->qd * d);
     RV_UP(ly.w[MAT_QKV] + (size_t)m->qd * d, w[2], (size_t)m->kvd * d);
     RV_UP(ly.w[MAT_QKV] + (size_t)(m->qd + m->kvd) * d, w[3], (size_t)m->kvd * d);
-    RV_ALLOC(A, ly.w[MAT_O], e2 * d * m->qd);
+    RV_ALLOC_W(A, ly.w[MAT_O], e2 * d * m->qd);
     RV_UP(ly.w[MAT_O], w[4], (size_t)d * m->qd);
-    RV_ALLOC(A, ly.w[MAT_GU], e2 * 2 * F * d);
+    RV_ALLOC_W(A, ly.w[MAT_GU], e2 * 2 * F * d);
     RV_UP(ly.w[MAT_GU], w[6], (size_t)F * d);
     RV_UP(ly.w[MAT_GU] + (size_t)F * d, w[7], (size_t)F * d);
-    RV_ALLOC(A, ly.w[MAT_D], e2 * d * F);
+    RV_ALLOC_W(A, ly.w[MAT_D], e2 * d * F);
     RV_UP(ly.w[MAT_D], w[8], (size_t)d * F);
   }
   // the one KV cache, filled with the sentinel
@@ -681,6 +712,7 @@ static int load_impl(rv_model *m, const rv_config *cfg, const void *const *weigh
   RV_ALLOC(A, m->gXf, sizeof(float) * (size_t)m->Bmax * d);
   RV_ALLOC(A, m->gLogits, sizeof(float) * (size_t)m->Bmax * V);
   RV_ALLOC(A, m->d_layers, sizeof(LayerDesc) * (size_t)m->L);
+  RV_ALLOC(A, m->d_tmaps, sizeof(CUtensorMap) * (size_t)(12 * m->L + 1));
   RV_ALLOC(A, m->bar, sizeof(unsigned) * 2);
   RV_CK(cudaMemsetAsync(m->bar, 0, sizeof(unsigned) * 2, m->stream));
   RV_CK(cudaStreamSynchronize(m->stream));
@@ -747,7 +779,7 @@ int rv_quantize_river(rv_model *m, int group_size, int entry_layer) {
       r.G = (mt.K + group_size - 1) / group_size;
       r.Gs = pad_groups(r.G);
       auto &A = m->river_allocs;
-      RV_ALLOC(A, r.q, sizeof(uint32_t) * (size_t)mt.N * (r.Kp / 8));
+      RV_ALLOC_W(A, r.q, sizeof(uint32_t) * (size_t)mt.N * (r.Kp / 8));
       RV_ALLOC(A, r.sz, sizeof(__half2) * (size_t)mt.N * r.Gs);
       if (r.Gs != r.G) RV_CK(cudaMemsetAsync(r.sz, 0, sizeof(__half2) * (size_t)mt.N * r.Gs, m->stream));
       if (m->quantizer == RV_QUANT_HQQ)

@@ -272,6 +272,8 @@ bool make_map(CUtensorMap *m, const void *p, int rows, int K, int act) {
 
 }  // namespace
 
+void *tensor_map_encoder() { return reinterpret_cast<void *>(encoder()); }
+
 bool gemm_tc_available() {
   int dev = 0, major = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;

@@ -144,6 +144,8 @@ cudaError_t launch_rmsnorm_rows(const float *H, const uint16_t *gamma, int d, fl
 // rows of X into xb [max_rows][K] (16-bit) and writes Y[list[r]][n];
 // K % 8 == 0.  Sets bit 16 of *err if a bounded wait gave up.
 bool gemm_tc_available();
+// The driver's cuTensorMapEncodeTiled (a PFN_cuTensorMapEncodeTiled_v12000), or NULL.
+void *tensor_map_encoder();
 cudaError_t launch_gemm_tc(const Mat &m, int act, const float *X, float *Y, const int32_t *list, const int32_t *count,
                            int max_rows, uint16_t *xb, int32_t *err, cudaStream_t s);
 // The same for an int4 river matrix: split into 16-bit hi + lo (whi, wlo:

@@ -3,13 +3,14 @@
 // the LM head and the greedy pick) in one cooperative launch with one block
 // per SM.
 //
-// Each block has PW producer warps and CW compute warps.
+// Each block has one producer warp and CW compute warps.
 //
-// Producers: walk the block's share of every weight matrix of the step in
-// consumption order (layer by layer: QKV, O, gate/up, down; then the LM
-// head) and copies it into a ring of shared-memory stages with bulk copies
-// (16-byte cp.async by every lane, completion signalled on the stage's
-// mbarrier).  A stage is one item: 16 rows x one 512-byte chunk of each row (1024 int4
+// Producer: one thread walks the block's share of every weight matrix of the
+// step in consumption order (layer by layer: QKV, O, gate/up, down; then the
+// LM head) and copies it into a ring of shared-memory stages with tensor
+// copies (TMA, completion counted in bytes on the stage's mbarrier; the
+// copies bypass the load/store path that the compute warps' shared-memory
+// reads use).  A stage is one item: 16 rows x one 512-byte chunk of each row (1024 int4
 // codes plus their (scale, zero) pairs, or 256 16-bit weights).  The
 // producer never waits on activations, only on free stages and, while the
 // token is still in the backbone, on the route of the next layer (published
@@ -22,14 +23,20 @@
 // their items: a row group of 16 rows is one mma.sync m16n8k16 row block,
 // with the activation chunk as column 0 of B (the other columns zero).
 //   16-bit path: A fragments straight from the stage (ldmatrix).
-//   int4 path: one shift and one LOP3 turn two codes of a word into two
-//   16-bit floats carrying the code in the low mantissa bits (bf16 128 + q,
-//   fp16 1 + q/16); lane (g, t) takes words t*w .. t*w + w - 1 of a block of
-//   4w words (one quantization group, w = group / 32) of rows g and g + 8,
-//   the k order inside the MMA follows the nibble order of the word and the
-//   activations are staged in the same order (pairs (x[8W+p], x[8W+p+4])).
-//   Per group, sum (q - z) x = A * D - (B + z) * X with X the group's
-//   activation sum, times the group's scale, into fp32 row sums.
+//   int4 path: a LOP3 turns two codes of a word into two fp16 values that
+//   carry them in their mantissa, 1024 + q (nibbles at bits 0..3 of each
+//   half: codes 8W, 8W+4 of word W) or 1024 + 16 q (bits 4..7: codes 8W+1,
+//   8W+5); one shift by 8 exposes the other four codes, so a word costs one
+//   shift and four LOP3s.  Lane (g, t) takes words t*w .. t*w + w - 1 of a
+//   block of 4w words (one quantization group, w = group / 32) of rows g
+//   and g + 8; the MMA's k order follows the nibbles, and the activations
+//   are staged in the same order as fp16 pairs (x[8W+p], x[8W+p+4]) (the
+//   model's 16-bit activations, exact in fp16 for |x| in [2^-14, 65504]).
+//   The even-k codes (1024 + q) and the odd-k codes (1024 + 16 q) go to two
+//   accumulators D0, D1; per group,
+//     sum (q - z) x = D0 + D1 / 16 - (1024 + z) X0 - (64 + z) X1
+//   with X0, X1 the group's activation sums over even and odd k, times the
+//   group's scale, into fp32 row sums.
 // Products of 16-bit values are exact; sums are fp32.  Row groups are split
 // over teams of warps; partial sums meet in shared memory in a fixed order;
 // the team's first warp runs the epilogue (RoPE + K/V append, residual,
@@ -56,6 +63,8 @@
 // paperlayer.ai summary section 4 (KV-Shared Exit Layer; Inference with
 // Seamless Exit) and aitrends.kr (s(l) = cos(h(l-1), h(l)) > tau; W4A16 exit
 // layers copied from the backbone blocks).
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "stream.cuh"
@@ -69,6 +78,23 @@ __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvt
 
 __device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *m, uint64_t *bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+          su32(dst)),
+      "l"(m), "r"(su32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *m, uint64_t *bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          su32(dst)),
+      "l"(m), "r"(su32(bar)), "r"(x), "r"(y)
+      : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
@@ -121,29 +147,18 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t m, uint32_t
   return d;
 }
 
-// Code extraction by activation type: pair j of a word holds the codes of
-// nibbles j and j + 4 (bf16: 128 + q at bits 0..3 / 16..19 after a shift by
-// 4j; fp16: 1 + q/16 at bits 6..9 / 22..25).  sum (q - z) x = CA acc - (CB + z) X.
-template <int ACT>
-struct Codes {
-  static constexpr uint32_t mask = ACT == 1 ? 0x000F000Fu : 0x03C003C0u;
-  static constexpr uint32_t one = ACT == 1 ? 0x43004300u : 0x3C003C00u;
-  static constexpr float CA = ACT == 1 ? 1.f : 16.f;
-  static constexpr float CB = ACT == 1 ? 128.f : 16.f;
-  __device__ __forceinline__ static void pairs(uint32_t w, uint32_t m, uint32_t o, uint32_t *p) {
-    if (ACT == 1) {
-      p[0] = lop3_and_or(w, m, o);
-      p[1] = lop3_and_or(w >> 4, m, o);
-      p[2] = lop3_and_or(w >> 8, m, o);
-      p[3] = lop3_and_or(w >> 12, m, o);
-    } else {
-      p[0] = lop3_and_or(w << 6, m, o);
-      p[1] = lop3_and_or(w << 2, m, o);
-      p[2] = lop3_and_or(w >> 2, m, o);
-      p[3] = lop3_and_or(w >> 6, m, o);
-    }
-  }
-};
+// int4 code extraction (fp16 for both activation types): from word w,
+//   p0 = codes (8W, 8W+4)   as 1024 + q      (bits 0..3 of each half)
+//   p1 = codes (8W+1, 8W+5) as 1024 + 16 q   (bits 4..7)
+//   p2, p3 the same for (8W+2, 8W+6), (8W+3, 8W+7) from w >> 8.
+constexpr uint32_t kNibLo = 0x000F000Fu, kNibHi = 0x00F000F0u, kF16_1024 = 0x64006400u;
+__device__ __forceinline__ void code_pairs(uint32_t w, uint32_t mlo, uint32_t mhi, uint32_t o, uint32_t *p) {
+  const uint32_t u = w >> 8;
+  p[0] = lop3_and_or(w, mlo, o);
+  p[1] = lop3_and_or(w, mhi, o);
+  p[2] = lop3_and_or(u, mlo, o);
+  p[3] = lop3_and_or(u, mhi, o);
+}
 
 // ---------------------------------------------------------------- shared state
 
@@ -261,82 +276,41 @@ __device__ __forceinline__ float3 csum3(const Shared &sh, float a, float b, floa
 // T (one per team); inside a round, chunk-major: (c = 0, teams 0..T-1),
 // (c = 1, ...), so every team's next chunk is close in the stream.
 
-__device__ __forceinline__ void cp_arrive_noinc(uint64_t *b) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(b)) : "memory");
-}
-
-// A producer warp: walks every item of the step in consumption order and
-// issues those with n % PW == pw (several warps keep more copies in
-// flight than one).  Lane 0 takes every wait and broadcasts its outcome, so
-// the warp's control flow stays uniform.  An item is copied by 16-byte cp.async (the load/store
-// path): lane L copies bytes 16L..16L+15 of every row's chunk, so each warp
-// instruction moves one contiguous row piece; the (scale, zero) pieces of an
-// int4 item follow.  Every lane then arms an arrive on the stage's barrier
-// (initialized to 32 arrivals) that fires when its copies have landed.
-__device__ void producer(const StreamArgs &A, const Shared &sh, int bid, int nb, int pw) {
-  const int lane = threadIdx.x & 31;
+// The producer: one thread walks every item of the step in consumption order
+// and copies each into its stage with tensor copies (TMA): two boxes of 8
+// rows x 512 bytes (rows 0..7 and 8..15 of the row group; the rows of a half
+// are consecutive matrix rows for every epilogue's row order), and for an
+// int4 item two boxes of the rows' (scale, zero) pairs.  The copies complete
+// on the stage's mbarrier in bytes; rows past the matrix arrive as zeros.
+__device__ void producer(const StreamArgs &A, const Shared &sh, int bid, int nb) {
+  if ((threadIdx.x & 31) != 0) return;
   const int NS = A.nstages;
   int n = 0, slot = 0;  // items issued; stage of the next item
   uint32_t ph = 0;      // parity of the next item's stage use
   bool stop = false;
   auto put = [&](const PhasePlan &p) {
-    const Mat &m = p.m;
-    const int Rb = p.j1 - p.j0, N = m.N, hd = A.hd;
-    // row pieces: source row stride, bytes per chunk (full / last), shared row stride
-    const bool river = p.river;
-    const unsigned char *wb = river ? reinterpret_cast<const unsigned char *>(m.r.q)
-                                    : reinterpret_cast<const unsigned char *>(m.w);
-    const size_t wrow = river ? (size_t)m.r.Kp / 2 : (size_t)m.K * 2;
-    const uint32_t wfull = 512, wlast = river ? (uint32_t)(m.r.Kp - (p.nk - 1) * CK4) / 2
-                                              : (uint32_t)(m.K - (p.nk - 1) * CK16) * 2;
-    const uint32_t srow_sm = river ? ROW4 : ROW16;
-    const int gpc = river ? CK4 / m.r.g : 0;
-    const unsigned char *sb = river ? reinterpret_cast<const unsigned char *>(m.r.sz) : nullptr;
-    const size_t szrow = river ? (size_t)m.r.Gs * 4 : 0;
-    const uint32_t sfull = gpc * 4, slast = river ? 4u * (uint32_t)((m.r.G - (p.nk - 1) * gpc + 3) & ~3) : 0u;
+    const int Rb = p.j1 - p.j0, N = p.m.N, hd = A.hd;
+    const int gpc = p.river ? CK4 / p.m.r.g : 0;
+    const uint32_t bytes = 2 * HALF_BYTES + (p.river ? (uint32_t)(2 * 8 * p.szw * 4) : 0u);
     for (int r0 = 0; r0 < Rb && !stop; r0 += p.T) {
       const int tr = min(p.T, Rb - r0);
       for (int c = 0; c < p.nk && !stop; ++c)
         for (int t = 0; t < tr; ++t) {
-          if (n % PW != pw) {  // another producer's item
-            ++n;
-            if (++slot == NS) {
-              slot = 0;
-              ph ^= 1u;
-            }
-            continue;
-          }
-          if (n >= NS) {
-            int ok = 1;
-            if (lane == 0) ok = wait_stage(sh, &sh.empty[slot], ph ^ 1u, A.st.err);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
-              stop = true;
-              break;
-            }
+          if (n >= NS && !wait_stage(sh, &sh.empty[slot], ph ^ 1u, A.st.err)) {
+            stop = true;
+            break;
           }
           const int j = p.j0 + r0 + t;
-          const bool last = c == p.nk - 1;
-          const uint32_t sd = su32(sh.ring + (size_t)slot * STAGE_BYTES);
-          if ((uint32_t)lane * 16 < (last ? wlast : wfull)) {
-            const unsigned char *src = wb + (size_t)c * 512 + lane * 16;
-#pragma unroll 4
-            for (int r = 0; r < RGR; ++r) {
-              const int row = rg_row(p.epi, j, r, N, hd);
-              if (row < N) cp16s(sd + r * srow_sm + lane * 16, src + (size_t)row * wrow);
-            }
+          const int row0 = rg_row(p.epi, j, 0, N, hd), row8 = rg_row(p.epi, j, 8, N, hd);
+          unsigned char *stage = sh.ring + (size_t)slot * STAGE_BYTES;
+          mbar_expect_tx(&sh.full[slot], bytes);
+          tma3d(stage, p.tm, &sh.full[slot], 0, row0, 4 * c);
+          tma3d(stage + HALF_BYTES, p.tm, &sh.full[slot], 0, row8, 4 * c);
+          if (p.river) {
+            tma2d(stage + SZ_OFF, p.tsz, &sh.full[slot], c * gpc, row0);
+            tma2d(stage + SZ_OFF + 8 * p.szw * 4, p.tsz, &sh.full[slot], c * gpc, row8);
           }
-          if (river) {
-            const int segs = (int)((last ? slast : sfull) >> 4);  // 16-byte pieces of a row's pairs
-            for (int q = lane; q < RGR * segs; q += 32) {
-              const int r = q / segs, k = q - r * segs;
-              const int row = rg_row(p.epi, j, r, N, hd);
-              if (row < N)
-                cp16s(sd + SZ_OFF + r * gpc * 4 + k * 16, sb + (size_t)row * szrow + (size_t)c * gpc * 4 + k * 16);
-            }
-          }
-          cp_arrive_noinc(&sh.full[slot]);
-          __syncwarp();
-          if (lane == 0) sh.issued[slot] = n;
+          sh.issued[slot] = n;
           ++n;
           if (++slot == NS) {
             slot = 0;
@@ -348,40 +322,40 @@ __device__ void producer(const StreamArgs &A, const Shared &sh, int bid, int nb,
   for (int l = 0; l < A.L && !stop; ++l) {
     // the route of layer l: known from the start (forced exits), after the
     // exit (the river to the end), or once the compute warps have decided
-    int ok = 1;
-    if (lane == 0) {
+    {
       const unsigned long long t0 = gtime();
       while (*sh.known <= l) {
         if (aborted(sh) || gtime() - t0 > kWaitNs) {
           if (!aborted(sh)) set_abort(sh, A.st.err, 32);
-          ok = 0;
+          stop = true;
           break;
         }
-        __nanosleep(64);
       }
+      if (stop) break;
       __threadfence_block();
-    }
-    if (!__shfl_sync(0xffffffffu, ok, 0)) {
-      stop = true;
-      break;
     }
     const int river = ((volatile int *)sh.routes)[l];
     const LayerDesc &ly = A.layers[l];
-    put(make_plan(ly.m[0], river, PH_QKV, bid, nb));
-    put(make_plan(ly.m[1], river, PH_O, bid, nb));
-    put(make_plan(ly.m[2], river, PH_GU, bid, nb));
-    put(make_plan(ly.m[3], river, PH_DOWN, bid, nb));
+    put(make_plan(ly.m[0], river, PH_QKV, bid, nb, ly.tw[0], ly.tq[0], ly.ts[0]));
+    put(make_plan(ly.m[1], river, PH_O, bid, nb, ly.tw[1], ly.tq[1], ly.ts[1]));
+    put(make_plan(ly.m[2], river, PH_GU, bid, nb, ly.tw[2], ly.tq[2], ly.ts[2]));
+    put(make_plan(ly.m[3], river, PH_DOWN, bid, nb, ly.tw[3], ly.tq[3], ly.ts[3]));
   }
   if (!stop) {
     Mat lm{};
     lm.w = A.lm_head;
     lm.N = A.V;
     lm.K = A.d;
-    put(make_plan(lm, 0, PH_HEAD, bid, nb));
+    put(make_plan(lm, 0, PH_HEAD, bid, nb, A.t_head));
   }
   // drain: no copy may still be in flight when the block exits
-  cp_wait<0>();
-  __syncwarp();
+  for (int m = n - NS < 0 ? 0 : n - NS; m < n; ++m) {
+    const unsigned q = (unsigned)m / (unsigned)NS;
+    const int sl = m - (int)q * NS;
+    const unsigned long long t0 = gtime();
+    while (!mbar_try(&sh.full[sl], q & 1u) && gtime() - t0 < kWaitNs) {
+    }
+  }
 }
 
 // ---------------------------------------------------------------- activation staging
@@ -396,13 +370,20 @@ template <int ACT>
 __device__ __forceinline__ void stage_word(int river, int t, int wpg, const float *x, unsigned char *xr, float *xs) {
   uint4 *xw = reinterpret_cast<uint4 *>(xr);
   if (river) {
+    // fp16 pairs (the values are already rounded to the model's 16-bit type;
+    // clamped to the fp16 range)
     uint32_t pr[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) pr[q] = (uint32_t)f_to_act(x[q], ACT) | ((uint32_t)f_to_act(x[q + 4], ACT) << 16);
+    for (int q = 0; q < 4; ++q)
+      pr[q] = (uint32_t)__half_as_ushort(__float2half_rn(fminf(fmaxf(x[q], -65504.f), 65504.f))) |
+              ((uint32_t)__half_as_ushort(__float2half_rn(fminf(fmaxf(x[q + 4], -65504.f), 65504.f))) << 16);
     xw[t] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-    float X = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
-    for (int o = 1; o < wpg; o <<= 1) X += __shfl_xor_sync(0xffffffffu, X, o);
-    if ((t & (wpg - 1)) == 0) xs[t / wpg] = X;
+    float X0 = (x[0] + x[2]) + (x[4] + x[6]), X1 = (x[1] + x[3]) + (x[5] + x[7]);
+    for (int o = 1; o < wpg; o <<= 1) {
+      X0 += __shfl_xor_sync(0xffffffffu, X0, o);
+      X1 += __shfl_xor_sync(0xffffffffu, X1, o);
+    }
+    if ((t & (wpg - 1)) == 0) reinterpret_cast<float2 *>(xs)[t / wpg] = make_float2(X0, X1);
   } else {
     xw[t] = make_uint4((uint32_t)f_to_act(x[0], ACT) | ((uint32_t)f_to_act(x[1], ACT) << 16),
                        (uint32_t)f_to_act(x[2], ACT) | ((uint32_t)f_to_act(x[3], ACT) << 16),
@@ -534,18 +515,27 @@ __device__ void stage_norm(const Shared &sh, const Mat &m, int river, const floa
 // ---------------------------------------------------------------- GEMV consumer
 
 // One group of an int4 item: the lane's w words of rows g and g + 8 against
-// the activation pairs, two MMA chains (even and odd word pairs) into d, e.
-template <int ACT, int W>
-__device__ __forceinline__ void group_mma(const uint32_t *r0, const uint32_t *r1, const uint4 *xp, int w0, bool col0,
-                                          uint32_t cm, uint32_t co, float *d, float *e) {
+// the activation pairs; even-k codes into d, odd-k codes into e (fp16 MMAs).
+// Byte offset of word w (0..127) of a row within its half of a stage (the
+// 128-byte swizzle: 16-byte unit u of row r sits at unit u ^ r).
+__device__ __forceinline__ int sw_word(int w, int r) {
+  return ((w >> 5) << 10) + (r << 7) + ((((w & 31) >> 2) ^ r) << 4) + ((w & 3) << 2);
+}
+
+template <int W>
+__device__ __forceinline__ void group_mma(const unsigned char *h0, const unsigned char *h1, int r, const uint4 *xp,
+                                          int w0, bool col0, uint32_t mlo, uint32_t mhi, uint32_t o, float *d,
+                                          float *e) {
   uint32_t wa[W], wb[W];
   if (W == 2) {
-    const uint2 a = *reinterpret_cast<const uint2 *>(r0 + w0), b = *reinterpret_cast<const uint2 *>(r1 + w0);
+    const int off = sw_word(w0, r);
+    const uint2 a = *reinterpret_cast<const uint2 *>(h0 + off), b = *reinterpret_cast<const uint2 *>(h1 + off);
     wa[0] = a.x; wa[1 % W] = a.y; wb[0] = b.x; wb[1 % W] = b.y;
   } else {
 #pragma unroll
     for (int i = 0; i < W; i += 4) {
-      const uint4 a = *reinterpret_cast<const uint4 *>(r0 + w0 + i), b = *reinterpret_cast<const uint4 *>(r1 + w0 + i);
+      const int off = sw_word(w0 + i, r);
+      const uint4 a = *reinterpret_cast<const uint4 *>(h0 + off), b = *reinterpret_cast<const uint4 *>(h1 + off);
       wa[i] = a.x; wa[(i + 1) % W] = a.y; wa[(i + 2) % W] = a.z; wa[(i + 3) % W] = a.w;
       wb[i] = b.x; wb[(i + 1) % W] = b.y; wb[(i + 2) % W] = b.z; wb[(i + 3) % W] = b.w;
     }
@@ -555,53 +545,56 @@ __device__ __forceinline__ void group_mma(const uint32_t *r0, const uint32_t *r1
     uint4 xv = make_uint4(0u, 0u, 0u, 0u);
     if (col0) xv = xp[w0 + i];
     uint32_t pa[4], pb[4];
-    Codes<ACT>::pairs(wa[i], cm, co, pa);
-    Codes<ACT>::pairs(wb[i], cm, co, pb);
-    float *acc = (i & 1) ? e : d;
-    mma16816<ACT>(acc, pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);
-    mma16816<ACT>(acc, pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
+    code_pairs(wa[i], mlo, mhi, o, pa);
+    code_pairs(wb[i], mlo, mhi, o, pb);
+    mma16816<0>(d, pa[0], pb[0], pa[2], pb[2], xv.x, xv.z);  // codes 8W+{0,4}, 8W+{2,6}
+    mma16816<0>(e, pa[1], pb[1], pa[3], pb[3], xv.y, xv.w);  // codes 8W+{1,5}, 8W+{3,7}
   }
 }
 
 // One int4 item (16 rows x one chunk) into the lane's row sums v0 (row g),
 // v1 (row g + 8); lanes with t == 0 hold the meaningful values.  Two groups
-// at a time, each on its own accumulators, so the MMAs of a group do not
-// wait on one another.
-template <int ACT, int W>
+// at a time, each on its own accumulators.
+__device__ __forceinline__ void item_int4_fold(const __half2 *szs, const float2 *xs2, int c, int gpc, int szw,
+                                               int blk, int gq, const float *d, const float *e, float &v0, float &v1) {
+  const float2 X = xs2[c * gpc + blk];
+  const float2 s0 = __half22float2(szs[gq * szw + blk]);
+  const float2 s1 = __half22float2(szs[(gq + 8) * szw + blk]);
+  const float b0 = fmaf(-(1024.f + s0.y), X.x, -(64.f + s0.y) * X.y);
+  const float b1 = fmaf(-(1024.f + s1.y), X.x, -(64.f + s1.y) * X.y);
+  v0 = fmaf(s0.x, fmaf(e[0], 0.0625f, d[0] + b0), v0);
+  v1 = fmaf(s1.x, fmaf(e[2], 0.0625f, d[2] + b1), v1);
+}
+
+template <int W>
 __device__ __forceinline__ void item_int4(const unsigned char *stage, const unsigned char *xr, const float *xs,
-                                          int c, int nwc, int gpc, float &v0, float &v1, int lane) {
+                                          int c, int nwc, int gpc, int szw, float &v0, float &v1, int lane) {
   const int gq = lane >> 2, tq = lane & 3;
-  uint32_t cm, co;
-  asm("mov.b32 %0, %1;" : "=r"(cm) : "n"(Codes<ACT>::mask));
-  asm("mov.b32 %0, %1;" : "=r"(co) : "n"(Codes<ACT>::one));
-  const uint32_t *r0 = reinterpret_cast<const uint32_t *>(stage + gq * ROW4);
-  const uint32_t *r1 = reinterpret_cast<const uint32_t *>(stage + (gq + 8) * ROW4);
+  uint32_t mlo, mhi, o;
+  asm("mov.b32 %0, %1;" : "=r"(mlo) : "n"(kNibLo));
+  asm("mov.b32 %0, %1;" : "=r"(mhi) : "n"(kNibHi));
+  asm("mov.b32 %0, %1;" : "=r"(o) : "n"(kF16_1024));
+  const unsigned char *h0 = stage, *h1 = stage + HALF_BYTES;  // rows gq and gq + 8 (row gq of each half)
   const uint4 *xp = reinterpret_cast<const uint4 *>(xr) + c * (CK4 / 8);
   const __half2 *szs = reinterpret_cast<const __half2 *>(stage + SZ_OFF);
+  const float2 *xs2 = reinterpret_cast<const float2 *>(xs);
   const int nblk = (nwc + 4 * W - 1) / (4 * W);
   const bool col0 = gq == 0;
-  auto fold = [&](int blk, const float *d, const float *e) {
-    const float X = xs[c * gpc + blk];
-    const float2 s0 = __half22float2(szs[gq * gpc + blk]);
-    const float2 s1 = __half22float2(szs[(gq + 8) * gpc + blk]);
-    v0 = fmaf(s0.x, fmaf(Codes<ACT>::CA, d[0] + e[0], -(Codes<ACT>::CB + s0.y) * X), v0);
-    v1 = fmaf(s1.x, fmaf(Codes<ACT>::CA, d[2] + e[2], -(Codes<ACT>::CB + s1.y) * X), v1);
-  };
   int blk = 0;
   for (; blk + 1 < nblk; blk += 2) {
     float d0[4] = {0.f, 0.f, 0.f, 0.f}, e0[4] = {0.f, 0.f, 0.f, 0.f};
     float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
-    group_mma<ACT, W>(r0, r1, xp, blk * 4 * W + tq * W, col0, cm, co, d0, e0);
-    group_mma<ACT, W>(r0, r1, xp, (blk + 1) * 4 * W + tq * W, col0, cm, co, d1, e1);
+    group_mma<W>(h0, h1, gq, xp, blk * 4 * W + tq * W, col0, mlo, mhi, o, d0, e0);
+    group_mma<W>(h0, h1, gq, xp, (blk + 1) * 4 * W + tq * W, col0, mlo, mhi, o, d1, e1);
     if (tq == 0) {
-      fold(blk, d0, e0);
-      fold(blk + 1, d1, e1);
+      item_int4_fold(szs, xs2, c, gpc, szw, blk, gq, d0, e0, v0, v1);
+      item_int4_fold(szs, xs2, c, gpc, szw, blk + 1, gq, d1, e1, v0, v1);
     }
   }
   if (blk < nblk) {
     float d0[4] = {0.f, 0.f, 0.f, 0.f}, e0[4] = {0.f, 0.f, 0.f, 0.f};
-    group_mma<ACT, W>(r0, r1, xp, blk * 4 * W + tq * W, col0, cm, co, d0, e0);
-    if (tq == 0) fold(blk, d0, e0);
+    group_mma<W>(h0, h1, gq, xp, blk * 4 * W + tq * W, col0, mlo, mhi, o, d0, e0);
+    if (tq == 0) item_int4_fold(szs, xs2, c, gpc, szw, blk, gq, d0, e0, v0, v1);
   }
 }
 
@@ -611,14 +604,19 @@ template <int ACT>
 __device__ __forceinline__ void item_16(const unsigned char *stage, const unsigned char *xr, int c, int nsteps,
                                         float *d, float *e, int lane) {
   const int gq = lane >> 2, tq = lane & 3;
-  const uint32_t a_addr = su32(stage) + (lane & 15) * ROW16 + (lane >> 4) * 16;
+  // ldmatrix: lane L gives row L & 15 (half (L & 15) >> 3, row r = L & 7 of
+  // it) at k offset 8 * (L >> 4) of the k-step; k-step s is 128-byte piece
+  // s >> 2, 16-byte unit 2 (s & 3) + (L >> 4), swizzled by r
+  const int r = lane & 7, hi = lane >> 4;
+  const uint32_t a_base = su32(stage) + ((lane & 15) >> 3) * HALF_BYTES + (r << 7);
+  auto a_addr = [&](int s) { return a_base + ((s >> 2) << 10) + (((((s & 3) << 1) | hi) ^ r) << 4); };
   const uint32_t *x32 = reinterpret_cast<const uint32_t *>(xr) + c * (CK16 / 2);
   int s = 0;
 #pragma unroll 2
   for (; s + 1 < nsteps; s += 2) {
     uint32_t a[4], b[4];
-    ldsm_x4(a, a_addr + s * 32);
-    ldsm_x4(b, a_addr + s * 32 + 32);
+    ldsm_x4(a, a_addr(s));
+    ldsm_x4(b, a_addr(s + 1));
     uint32_t x0 = 0u, x1 = 0u, x2 = 0u, x3 = 0u;
     if (gq == 0) {
       x0 = x32[s * 8 + tq];
@@ -631,7 +629,7 @@ __device__ __forceinline__ void item_16(const unsigned char *stage, const unsign
   }
   if (s < nsteps) {
     uint32_t a[4];
-    ldsm_x4(a, a_addr + s * 32);
+    ldsm_x4(a, a_addr(s));
     uint32_t x0 = 0u, x1 = 0u;
     if (gq == 0) {
       x0 = x32[s * 8 + tq];
@@ -727,9 +725,9 @@ __device__ int consume(const StreamArgs &A, const Shared &sh, const PhasePlan &p
         const unsigned char *stg = sh.ring + (size_t)slot * STAGE_BYTES;
         if (p.river) {
           const int nwc = min(CK4, p.m.r.Kp - c * CK4) / 8;
-          if (W == 4) item_int4<ACT, 4>(stg, sh.xr, xs, c, nwc, gpc, y0, y1, lane);
-          else if (W == 2) item_int4<ACT, 2>(stg, sh.xr, xs, c, nwc, gpc, y0, y1, lane);
-          else item_int4<ACT, 8>(stg, sh.xr, xs, c, nwc, gpc, y0, y1, lane);
+          if (W == 4) item_int4<4>(stg, sh.xr, xs, c, nwc, gpc, p.szw, y0, y1, lane);
+          else if (W == 2) item_int4<2>(stg, sh.xr, xs, c, nwc, gpc, p.szw, y0, y1, lane);
+          else item_int4<8>(stg, sh.xr, xs, c, nwc, gpc, p.szw, y0, y1, lane);
         } else {
           item_16<ACT>(stg, sh.xr, c, min(CK16, p.m.K - c * CK16) / 16, d, d2, lane);
         }
@@ -924,7 +922,9 @@ __device__ void attn_task(const StreamArgs &A, const Shared &sh, int l, int task
 
 template <int ACT, int HD, int GRP>
 __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // the swizzled tensor boxes need 1024-byte aligned stages
+  unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int NS = A.nstages;
   Shared sh;
   sh.ring = smem;
@@ -945,7 +945,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
   const int L = A.L;
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&sh.full[i], 32);  // one arrive per producer lane, when its copies have landed
+      mbar_init(&sh.full[i], 1);   // the producer's arrive (with the item's byte count)
       mbar_init(&sh.empty[i], 1);  // the consuming warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -972,14 +972,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
   }
   __syncthreads();
 
-  if (warp >= CW) {  // ------------------------------------------------ producers
-    producer(A, sh, bid, nb, warp - CW);
+  if (warp == CW) {  // ------------------------------------------------ producer
+    producer(A, sh, bid, nb);
     return;
   }
 
   // ------------------------------------------------------------------ compute warps
   unsigned epoch = 0;
   const int pos = A.st.len[0];
+  const DecideScalars dsc = load_decide_scalars(A.st, 0);  // read once: the decisions wait on no memory
   // the route and exit layer as the decisions below update them (forced
   // exit 0: every layer in the river)
   int route = 0, exit_l = L;
@@ -1015,12 +1016,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
       float3 ds = make_float3(0.f, 0.f, 0.f);
       const bool decide_now = l > 0 && route == 0;
       // stage for the route before the decision; re-stage if it flips
-      PhasePlan p = make_plan(ly.m[0], route, PH_QKV, bid, nb);
+      PhasePlan p = make_plan(ly.m[0], route, PH_QKV, bid, nb, ly.tw[0], ly.tq[0], ly.ts[0]);
       stage_norm<ACT>(sh, p.m, p.river, hin, ly.attn_norm, A.eps, decide_now ? A.h[(l - 1) & 1] : nullptr,
                       decide_now ? &ds : nullptr, sh.xr);
       if (l > 0) {
         if (decide_now) {
-          const Decision dc = decide(A.st, 0, 0, l, L, ds.x, ds.y, ds.z);
+          const Decision dc = decide(dsc, 0, l, L, ds.x, ds.y, ds.z);
           if (bid == 0 && tid == 0 && A.dbg_s) A.dbg_s[(size_t)(l - 1) * A.Bmax] = dc.s;
           if (dc.exited) {
             route = 1;
@@ -1037,7 +1038,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
       }
       cbar();
       if (p.river != (route || !ly.m[0].w ? 1 : 0)) {
-        p = make_plan(ly.m[0], route, PH_QKV, bid, nb);
+        p = make_plan(ly.m[0], route, PH_QKV, bid, nb, ly.tw[0], ly.tq[0], ly.ts[0]);
         stage_norm<ACT>(sh, p.m, p.river, hin, ly.attn_norm, A.eps, nullptr, nullptr, sh.xr);
         cbar();
       }
@@ -1062,7 +1063,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
     grid_barrier(sh, A.bar, epoch, A.st.err);
     // ---- O + residual
     {
-      PhasePlan p = make_plan(ly.m[1], route, PH_O, bid, nb);
+      PhasePlan p = make_plan(ly.m[1], route, PH_O, bid, nb, ly.tw[1], ly.tq[1], ly.ts[1]);
       stage_vec<ACT>(p.m, p.river, A.o, sh.xr);
       cbar();
       Epi e{l, pos, hin, A.hmid, nullptr, 0.f, 0};
@@ -1071,7 +1072,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
     grid_barrier(sh, A.bar, epoch, A.st.err);
     // ---- gate/up + SwiGLU
     {
-      PhasePlan p = make_plan(ly.m[2], route, PH_GU, bid, nb);
+      PhasePlan p = make_plan(ly.m[2], route, PH_GU, bid, nb, ly.tw[2], ly.tq[2], ly.ts[2]);
       stage_norm<ACT>(sh, p.m, p.river, A.hmid, ly.mlp_norm, A.eps, nullptr, nullptr, sh.xr);
       cbar();
       Epi e{l, pos, nullptr, nullptr, nullptr, 0.f, 0};
@@ -1080,7 +1081,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
     grid_barrier(sh, A.bar, epoch, A.st.err);
     // ---- down + residual
     {
-      PhasePlan p = make_plan(ly.m[3], route, PH_DOWN, bid, nb);
+      PhasePlan p = make_plan(ly.m[3], route, PH_DOWN, bid, nb, ly.tw[3], ly.tq[3], ly.ts[3]);
       stage_vec<ACT>(p.m, p.river, A.a, sh.xr);
       cbar();
       Epi e{l, pos, A.hmid, hout, A.dbg_h ? A.dbg_h + (size_t)(l + 1) * A.Bmax * A.d : nullptr, 0.f, 0};
@@ -1100,7 +1101,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
       n2 = fmaf(y, y, n2);
     }
     const float3 t3 = csum3(sh, dot, n1, n2);
-    const Decision dc = decide(A.st, 0, route, L, L, t3.x, t3.y, t3.z);
+    const Decision dc = decide(dsc, route, L, L, t3.x, t3.y, t3.z);
     if (tid == 0) A.dbg_s[(size_t)(L - 1) * A.Bmax] = dc.s;
   }
 
@@ -1109,7 +1110,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
   lm.w = A.lm_head;
   lm.N = A.V;
   lm.K = A.d;
-  PhasePlan ph = make_plan(lm, 0, PH_HEAD, bid, nb);
+  PhasePlan ph = make_plan(lm, 0, PH_HEAD, bid, nb, A.t_head);
   stage_norm<ACT>(sh, ph.m, 0, A.h[L & 1], A.final_norm, A.eps, nullptr, nullptr, sh.xr);
   cbar();
   Epi e{L, pos, nullptr, nullptr, nullptr, -INFINITY, 0x7fffffff};
@@ -1185,7 +1186,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
 namespace {
 
 size_t stream_smem(const StreamArgs &A) {
-  return (size_t)A.nstages * sk::STAGE_BYTES + A.xbytes + sizeof(float) * (2 * sk::CW * 16 + 128) +
+  return 1024 + (size_t)A.nstages * sk::STAGE_BYTES + A.xbytes + sizeof(float) * (2 * sk::CW * 16 + 128) +
          2 * sizeof(uint64_t) * A.nstages + sizeof(int) * (4 + A.nstages + A.L);
 }
 
@@ -1230,6 +1231,40 @@ cudaError_t launch_t(const StreamArgs &A, int grid, cudaStream_t s) {
 }
 
 }  // namespace
+
+bool stream_map_w16(CUtensorMap *t, const void *w, int N, int K, int act) {
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+  if (!enc || !w || N < 1 || K < 8) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)N, (cuuint64_t)((K + 63) / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};
+  cuuint32_t box[3] = {64, 8, 4}, es[3] = {1, 1, 1};
+  return enc(t, act == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(w),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool stream_map_q(CUtensorMap *t, const void *q, int N, int Kp) {
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+  if (!enc || !q || N < 1 || Kp < 32) return false;
+  cuuint64_t dims[3] = {32, (cuuint64_t)N, (cuuint64_t)((Kp / 8 + 31) / 32)};
+  cuuint64_t strides[2] = {(cuuint64_t)Kp / 2, 128};
+  cuuint32_t box[3] = {32, 8, 4}, es[3] = {1, 1, 1};
+  return enc(t, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(q), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool stream_map_sz(CUtensorMap *t, const void *sz, int N, int Gs, int g) {
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+  if (!enc || !sz || N < 1 || Gs < 4 || g < 64) return false;
+  const int gpc = sk::CK4 / g, w = gpc < Gs ? gpc : Gs;
+  cuuint64_t dims[2] = {(cuuint64_t)Gs, (cuuint64_t)N};
+  cuuint64_t strides[1] = {(cuuint64_t)Gs * 4};
+  cuuint32_t box[2] = {(cuuint32_t)w, 8}, es[2] = {1, 1};
+  return enc(t, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(sz), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 #define RV_STREAM_DISPATCH(CALL)                                      \
   const int grp = A.H / A.Hkv;                                        \

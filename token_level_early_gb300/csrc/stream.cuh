@@ -3,20 +3,24 @@
 // and the host entry points.  Internal header.
 #pragma once
 
+#include <cuda.h>
+
 #include "kernels.cuh"
 
 namespace rv {
 namespace sk {
 
 constexpr int CW = 8;              // compute warps per block
-constexpr int PW = 8;              // producer warps per block (item n goes to producer n % PW)
-constexpr int NTHREADS = (CW + PW) * 32;
+constexpr int NTHREADS = (CW + 1) * 32;  // + one producer warp (one thread issues the tensor copies)
 constexpr int RGR = 16;            // rows per row group (the MMA's M)
 constexpr int CK4 = 1024;          // int4 codes per chunk (512 bytes of a row)
 constexpr int CK16 = 256;          // 16-bit weights per chunk (512 bytes of a row)
-constexpr int ROW4 = 576;          // shared-memory row stride of an int4 stage (512 + 64 bytes)
-constexpr int ROW16 = 528;         // shared-memory row stride of a 16-bit stage (512 + 16 bytes)
-constexpr int SZ_OFF = RGR * ROW4;           // (scale, zero) rows of an int4 stage
+// A stage holds one item as two tensor boxes of 8 rows x 4 x 128 bytes
+// (rows 0..7 then 8..15 of the row group), each laid out [128-byte piece q]
+// [row r][128 bytes] with the 128-byte swizzle (16-byte unit u of row r at
+// unit u ^ r); for int4 the rows' (scale, zero) pairs follow.
+constexpr int HALF_BYTES = 4096;
+constexpr int SZ_OFF = 2 * HALF_BYTES;
 constexpr int STAGE_BYTES = SZ_OFF + RGR * 64;  // room for 16 groups per row and chunk (g >= 64)
 constexpr int MAX_STAGES = 24;
 constexpr int ATILE = 32;          // attention positions per K/V tile
@@ -28,12 +32,16 @@ enum { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_DOWN = 3, PH_HEAD = 4 };
 // One decoder layer as the persistent kernel sees it (device array [L]).
 struct LayerDesc {
   Mat m[4];  // fused QKV, O, fused gate/up, down (16-bit + river copy)
+  // tensor maps (device memory) of each matrix: 16-bit weights, int4 codes,
+  // (scale, zero) pairs; NULL where the matrix does not exist
+  const CUtensorMap *tw[4], *tq[4], *ts[4];
   const uint16_t *attn_norm, *mlp_norm;
 };
 
 struct StreamArgs {
   const LayerDesc *layers;  // [L]
   const uint16_t *embed, *final_norm, *lm_head;
+  const CUtensorMap *t_head;  // the LM head's tensor map
   int L, d, H, Hkv, hd, F, V, act, Bmax;
   float eps;
   KVGeom kv;
@@ -58,6 +66,8 @@ struct PhasePlan {
   int river;   // 1: int4 river copy, 0: 16-bit backbone matrix
   int epi;     // sk::PH_*
   int R, nk, j0, j1, S, T;
+  const CUtensorMap *tm, *tsz;  // weights (16-bit or int4 codes), (scale, zero) pairs
+  int szw;                      // (scale, zero) pairs per row in a stage (int4)
 };
 
 // Matrix row of row r (0..15) of row group j.  QKV: 8 consecutive rotary
@@ -96,10 +106,15 @@ __host__ __device__ __forceinline__ void pick_team(int rmax, int nk, int &S, int
   T = sk::CW / S;
 }
 
-__host__ __device__ __forceinline__ PhasePlan make_plan(const Mat &m, int river, int epi, int bid, int nb) {
+__host__ __device__ __forceinline__ PhasePlan make_plan(const Mat &m, int river, int epi, int bid, int nb,
+                                                      const CUtensorMap *tw = nullptr, const CUtensorMap *tq = nullptr,
+                                                      const CUtensorMap *ts = nullptr) {
   PhasePlan p;
   p.m = m;
   p.river = (river || !m.w) ? 1 : 0;  // an offloaded backbone layer exists only in the river
+  p.tm = p.river ? tq : tw;
+  p.tsz = ts;
+  p.szw = p.river ? (sk::CK4 / m.r.g < m.r.Gs ? sk::CK4 / m.r.g : m.r.Gs) : 0;
   p.epi = epi;
   p.R = row_groups(epi, m.N);
   p.nk = p.river ? (m.r.Kp + sk::CK4 - 1) / sk::CK4 : (m.K + sk::CK16 - 1) / sk::CK16;
@@ -111,8 +126,9 @@ __host__ __device__ __forceinline__ PhasePlan make_plan(const Mat &m, int river,
 
 // Activations of a phase staged in shared memory: words of 8 values (16 bytes
 // as 16-bit), a whole number of warps of them.  16-bit path: the vector in
-// natural order; int4 path: pair words (x[8W+p], x[8W+p+4]), p = 0..3, zero
-// beyond K up to whole groups, then the groups' activation sums (floats).
+// natural order, in the model's 16-bit type; int4 path: pair words
+// (x[8W+p], x[8W+p+4]), p = 0..3, as fp16, zero beyond K up to whole groups,
+// then per group the activation sums over even and odd k (two floats).
 struct XGeom {
   int nw_valid;  // words holding activations
   int nw;        // words staged (a multiple of 32)
@@ -128,7 +144,7 @@ __host__ __device__ __forceinline__ XGeom x_geom(const Mat &m, int river) {
     x.nw = ((kg / 8) + 31) & ~31;
     x.wpg = g / 8;
     x.xs_off = x.nw * 16;
-    x.bytes = x.xs_off + 4 * (((x.nw / x.wpg) + 3) & ~3);
+    x.bytes = x.xs_off + 8 * (((x.nw / x.wpg) + 3) & ~3);
   } else {
     x.nw = (x.nw_valid + 31) & ~31;
     x.wpg = 1;
@@ -137,6 +153,14 @@ __host__ __device__ __forceinline__ XGeom x_geom(const Mat &m, int river) {
   }
   return x;
 }
+
+// Tensor maps of the persistent engine (false if the driver refuses one):
+// 16-bit weights [N][K] and int4 codes [N][Kp/8] as 3-D tensors (128-byte
+// piece, row, piece index) with 8 x 4 x 128-byte boxes and the 128-byte
+// swizzle; (scale, zero) pairs [N][Gs] as 2-D with min(1024 / g, Gs) x 8 boxes.
+bool stream_map_w16(CUtensorMap *t, const void *w, int N, int K, int act);
+bool stream_map_q(CUtensorMap *t, const void *q, int N, int Kp);
+bool stream_map_sz(CUtensorMap *t, const void *sz, int N, int Gs, int g);
 
 cudaError_t stream_prepare(StreamArgs &A, int n_sm, int *grid);
 cudaError_t stream_launch(const StreamArgs &A, int grid, cudaStream_t s);
