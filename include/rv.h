@@ -49,7 +49,7 @@ extern "C" {
 #define RV_ECUDA (-3)      /* a CUDA runtime call failed */
 #define RV_ECAPACITY (-4)  /* a row's KV cache is full (len == max_seq); nothing changed */
 #define RV_ESTATE (-5)     /* call out of order, e.g. tau-rule decode before rv_quantize_river */
-#define RV_ETIMEOUT (-6)   /* a bounded device wait gave up (persistent engine grid barrier) */
+#define RV_ETIMEOUT (-6)   /* a bounded device wait gave up (persistent engine, tensor-core GEMM) */
 
 /* Projection ids of a decoder layer (for rv_export_river). */
 #define RV_PROJ_Q 0
@@ -173,7 +173,22 @@ int rv_debug_dump(rv_model *m, int what, void *dst, size_t bytes);
 #define RV_OPT_QUANTIZER 1
 #define RV_QUANT_RTN 0
 #define RV_QUANT_HQQ 1
+/* RV_OPT_WAIT_LIMIT_US: the limit, in microseconds, of every bounded device
+ * wait of the persistent kernel (grid barriers, weight-ring stages, route
+ * hand-offs); 0 restores the default of two seconds.  A wait that runs out
+ * sets an error flag; the kernel finishes its control flow without waiting,
+ * lets its copies land, returns, and the step reports RV_ETIMEOUT without
+ * advancing the cached positions.  A limit of a few microseconds makes
+ * waits run out on purpose (a test of that path). */
+#define RV_OPT_WAIT_LIMIT_US 2
 int rv_set_option(rv_model *m, int option, int value);
+
+/* Test hook: make a device allocation of this library fail.  after >= 0:
+ * the next `after` allocations (cudaMalloc) succeed and the one after them
+ * fails as if the device were out of memory (once); after < 0 turns the hook
+ * off.  Process-wide; returns RV_OK.  The failing call returns RV_ENOMEM and
+ * frees what it had allocated. */
+int rv_debug_fail_alloc(int after);
 
 /* Kernel timing for roofline reports: launch one batch-1 GEMV kernel of the
  * decode step `iters` times back to back on the model's stream (outside the
@@ -205,9 +220,11 @@ int rv_time_kernel(rv_model *m, int kind, int layer, int river, int iters, float
  * device looks the array's address up (cudaGetSymbolAddress), so make that
  * first call before any stream capture.  All calls share the one array:
  * calls whose executions overlap on the GPU (other streams, other threads)
- * race and must be serialized by the caller.  Returns RV_EINVAL for
- * vocab not a positive multiple of 4, d_model not a positive multiple of 8
- * or d_model above the maximum of 16384. */
+ * race and must be serialized by the caller.  Returns RV_EINVAL, before
+ * any GPU work, for vocab not a positive multiple of 4, d_model not a
+ * positive multiple of 8, d_model above the maximum of 16384, vocab x
+ * d_model above 2^32 - 1, or d_lm_head, d_final_norm or d_h not 16-byte
+ * aligned (the kernel reads them with 16-byte loads). */
 int rv_greedy_head_noalloc(const void *d_lm_head, const void *d_final_norm, const float *d_h, int vocab,
                            int d_model, int act_dtype, float rms_eps, int32_t *d_next_id, float *d_logits,
                            void *stream);

@@ -58,3 +58,28 @@ def test_every_entry_point_rejects_a_null_handle():
     assert lib.rv_time_kernel(None, rv.TIME_GATEUP, 1, 0, 1, C.byref(ms), C.byref(by)) == E
     assert lib.rv_greedy_head_noalloc(None, None, None, 8, 8, 1, C.c_float(1e-5), None, None, None) == E
     assert b"null" in lib.rv_last_error()
+
+
+def test_noalloc_head_checks_sizes_and_alignment_before_any_gpu_work():
+    """rv_greedy_head_noalloc validates every argument before it touches the
+    GPU: sizes beyond its limits (including vocab x d_model beyond the GEMV's
+    32-bit offsets) and pointers that are not 16-byte aligned come back as
+    RV_EINVAL, on a machine without a GPU."""
+    import ctypes as C
+
+    lib = rv.lib()
+    E = rv.RV_EINVAL
+    ok, odd = 0x10000, 0x10004  # never dereferenced: the checks come first
+    eps = C.c_float(1e-5)
+    cases = [
+        (ok, ok, ok, 262144, 16384),  # 2^32 elements
+        (ok, ok, ok, 6, 256),         # vocab not a multiple of 4
+        (ok, ok, ok, 1024, 12),       # d_model not a multiple of 8
+        (ok, ok, ok, 1024, 16392),    # d_model above 16384
+        (odd, ok, ok, 1024, 256),     # misaligned LM head
+        (ok, odd, ok, 1024, 256),     # misaligned gain
+        (ok, ok, odd, 1024, 256),     # misaligned hidden state
+    ]
+    for head, norm, h, vocab, dm in cases:
+        assert lib.rv_greedy_head_noalloc(head, norm, h, vocab, dm, 1, eps, ok, None, None) == E, (vocab, dm)
+        assert lib.rv_last_error()

@@ -96,3 +96,82 @@ def test_lp_error_below_rtn(act):
         abs_h += float(np.abs(eh).mean())
         abs_r += float(np.abs(er).mean())
     assert lp_h < lp_r and abs_h < abs_r, (lp_h, lp_r, abs_h, abs_r)
+
+
+def hqq_zeros_fp64(x, s, p=0.7, beta=10.0, kappa=1.01, iters=20, tie=1e-6):
+    """The HQQ zero-point iteration (Badri and Shaji 2023) restated in fp64
+    with the mathematical power, for a fixed scale s: codes from the current
+    zero, residual, the lp shrink of the residual, the zero as the mean of
+    q - (w - e) / s, beta grows by kappa, and the loop stops once the mean
+    absolute residual of an iteration is not below the best so far (that
+    iteration's zero is kept).  When the codes repeat, two iterations have
+    the same mean residual and the stopping test is a tie that fp32 and fp64
+    sums may resolve either way; every zero reachable by resolving such ties
+    (within `tie`, relative) either way is returned."""
+    x = np.asarray(x, dtype=np.float64)
+    out = set()
+
+    def run(z, beta, best, it):
+        while it < iters:
+            q = np.clip(np.rint(x / s + z), 0, 15)
+            res = x - (q - z) * s
+            a = np.abs(res)
+            with np.errstate(divide="ignore"):
+                shrunk = np.where(a > 0, a - np.power(np.where(a > 0, a, 1.0), p - 1) / beta, 0.0)
+            e = np.sign(res) * np.maximum(shrunk, 0.0)
+            z = float(np.mean(q - (x - e) / s))
+            beta *= kappa
+            it += 1
+            err = float(a.mean())
+            if math.isfinite(best) and abs(err - best) <= tie * best:
+                out.add(z)  # stop here ...
+                best = min(best, err)  # ... or go on
+                continue
+            if err < best:
+                best = err
+            else:
+                out.add(z)
+                return
+        out.add(z)
+
+    run(-x.min() / s, beta, math.inf, 0)
+    return sorted(out)
+
+
+def f16_ulp(v):
+    v = abs(float(v))
+    return 2.0 ** (math.floor(math.log2(v)) - 10) if v >= 2.0 ** -14 else 2.0 ** -24
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_hqq_zero_matches_fp64_restatement(act):
+    """The oracle's fp16 zero equals an independent fp64 restatement of the
+    iteration to within one fp16 step (fp32 against fp64 sums may move a
+    rint across .5; ties of the stopping test may go either way); a wrong
+    shrink sign, beta schedule or start moves it by many steps.  Its codes
+    are the round-to-nearest of w / s + z for the stored zero."""
+    rng = np.random.default_rng(17)
+    exact = 0
+    n_groups = 120
+    for g in range(n_groups):
+        n = (128, 64, 37)[g % 3]
+        # at sigma 0.02 every residual is far below |r|^(p-1) / beta, so the
+        # shrink returns zero and only the mean update acts; at sigma 1 and 5
+        # the shrink is active (|r|^(1-p) > 1 / beta), which pins its sign and
+        # the beta schedule
+        sigma = (0.02, 1.0, 5.0)[(g // 3) % 3]
+        bits = to_bits(rng.normal(0, sigma, n).astype(np.float32), act)
+        x = bits_to_f(bits, act)
+        qh, sh, zh, rc = oracle.hqq_group(bits, act)
+        assert rc == 0
+        s = h2f(sh)
+        zs = [float(np.float16(z)) for z in hqq_zeros_fp64(x, s)]
+        zo = h2f(zh)
+        near = min(abs(zo - z16) for z16 in zs)
+        assert near <= f16_ulp(abs(zo)) * 1.0001, (g, zo, zs)
+        exact += zo in zs
+        t = x / s + zo
+        ties = np.abs(t - np.floor(t) - 0.5) < 1e-6
+        want = np.clip(np.rint(t), 0, 15)
+        assert np.array_equal(qh[~ties], want[~ties].astype(qh.dtype)), g
+    assert exact >= 0.9 * n_groups, exact

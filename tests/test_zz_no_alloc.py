@@ -8,6 +8,7 @@ the array the first one left behind).  This file is collected last."""
 import numpy as np
 import pytest
 
+import oracle
 import synth
 import token_level_early_gb300 as rv
 
@@ -55,3 +56,42 @@ def test_noalloc_head_rejects_sizes_beyond_its_limits():
         with pytest.raises(rv.RVError) as e:
             rv.greedy_head_noalloc(p, p, p, vocab, dm, 1, 1e-5, p, None, None)
         assert e.value.code == rv.RV_EINVAL
+
+
+@pytest.mark.parametrize("d_model,vocab", [(16384, 1024), (264, 256)])
+def test_noalloc_head_synthetic_shapes_against_oracle(d_model, vocab):
+    """Shapes no model of the decode step uses: the advertised maximum width
+    (16384) and a width that is a multiple of 8 but not of 32.  Random hidden
+    state, RMSNorm gain and LM head; the greedy id must equal the oracle's
+    (unless the oracle's top two logits are within 1e-2) and the logits must
+    agree within 5e-2."""
+    import torch
+
+    shape = synth.ModelShape(f"head-{d_model}", 1, d_model, 1, 1, 8, 8, vocab, 0, synth.BF16)
+    w = synth.make_weights(shape, seed=21)
+    rng = np.random.default_rng(5)
+    gain = (1.0 + 0.1 * rng.standard_normal(d_model)).astype(np.float32)
+    w[1] = (gain.view(np.uint32) >> 16).astype(np.uint16)  # bf16 bits (truncated: any 16-bit value will do)
+    h = rng.standard_normal((1, d_model)).astype(np.float32)
+    om = oracle.Model(shape, w, 1, 2)
+    ol, oid = om.head(h.astype(np.float64))
+    om.close()
+    d_head = torch.from_numpy(w[2].view(np.int16)).cuda()
+    d_norm = torch.from_numpy(w[1].view(np.int16)).cuda()
+    d_h = torch.from_numpy(h[0].copy()).cuda()
+    d_next = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    d_logits = torch.zeros(vocab, dtype=torch.float32, device="cuda")
+    for _ in range(2):  # two calls in a row on the shared scratch array
+        d_next.fill_(-1)
+        torch.cuda.synchronize()
+        rv.greedy_head_noalloc(d_head.data_ptr(), d_norm.data_ptr(), d_h.data_ptr(), vocab, d_model, synth.BF16,
+                               shape.rms_eps, d_next.data_ptr(), d_logits.data_ptr(),
+                               torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        logits = d_logits.cpu().numpy()
+        assert np.abs(logits - ol[0]).max() <= 5e-2
+        top2 = np.sort(ol[0])[-2:]
+        if top2[1] - top2[0] >= 1e-2:
+            assert int(d_next.item()) == int(oid[0])
+        else:
+            assert ol[0][int(d_next.item())] >= top2[1] - 1e-2

@@ -29,9 +29,10 @@ DUMP_HIDDEN, DUMP_S, DUMP_LOGITS, DUMP_KV, DUMP_LENS = range(5)
 EXPORTED = ("rv_last_error", "rv_load_model", "rv_quantize_river", "rv_export_river", "rv_prefill",
             "rv_decode_step", "rv_decode_step_dev", "rv_sync_status", "rv_kv_reset", "rv_set_debug",
             "rv_debug_dump", "rv_kv_bytes", "rv_param_bytes", "rv_free_model", "rv_time_kernel", "rv_greedy_head_noalloc", "rv_offload_backbone",
-            "rv_set_option")
+            "rv_set_option", "rv_debug_fail_alloc")
 OPT_DECODE_ENGINE, ENGINE_CHAIN, ENGINE_PERSISTENT = 0, 0, 1
 OPT_QUANTIZER, QUANT_RTN, QUANT_HQQ = 1, 0, 1
+OPT_WAIT_LIMIT_US = 2
 TIME_GATEUP, TIME_O, TIME_LMHEAD = 0, 1, 2
 
 
@@ -122,6 +123,7 @@ def lib():
                             ctypes.POINTER(ctypes.c_double)], i32),
         "rv_greedy_head_noalloc": ([vp, vp, vp, i32, i32, i32, f32, vp, vp, vp], i32),
         "rv_set_option": ([vp, i32, i32], i32),
+        "rv_debug_fail_alloc": ([i32], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -145,6 +147,12 @@ def greedy_head_noalloc(d_lm_head: int, d_final_norm: int, d_h: int, vocab: int,
     """rv_greedy_head_noalloc on device pointers (see include/rv.h)."""
     _check(lib().rv_greedy_head_noalloc(d_lm_head, d_final_norm, d_h, vocab, d_model, act_dtype, float(rms_eps),
                                         d_next_id, d_logits, stream))
+
+
+def debug_fail_alloc(after: int) -> None:
+    """Test hook: the device allocation after the next `after` ones fails
+    (once); after < 0 turns it off (rv_debug_fail_alloc)."""
+    _check(lib().rv_debug_fail_alloc(int(after)))
 
 
 def config_of(shape, max_batch: int, max_seq: int) -> RVConfig:

@@ -12,6 +12,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <map>
 #include <string>
 #include <algorithm>
@@ -125,6 +126,7 @@ struct rv_model {
 
   // persistent batch-1 step (stream.cu)
   int engine = RV_ENGINE_CHAIN;
+  int wait_us = 0;  // RV_OPT_WAIT_LIMIT_US (0: the kernel's default)
   bool stream_ready = false;
   int stream_grid = 0;
   LayerDesc *d_layers = nullptr;
@@ -135,9 +137,14 @@ struct rv_model {
 
 namespace {
 
+// Test hook (rv_debug_fail_alloc): allocations left before one fails; < 0 off.
+std::atomic<long> g_fail_after{-1};
+
 int dalloc(rv_model *m, std::vector<void *> &list, void **p, size_t bytes) {
   *p = nullptr;
   if (bytes == 0) bytes = 16;
+  if (g_fail_after.load() >= 0 && g_fail_after.fetch_sub(1) == 0)
+    return fail(RV_ENOMEM, "cudaMalloc(%zu bytes) failed: injected by rv_debug_fail_alloc", bytes);
   cudaError_t e = cudaMalloc(p, bytes);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -511,6 +518,7 @@ int build_stream(rv_model *m) {
   A.dbg_s = m->debug ? m->dbg_s : nullptr;
   A.dbg_logits = m->debug ? m->dbg_logits : nullptr;
   A.xbytes = xb;
+  A.wait_ns = (unsigned long long)m->wait_us * 1000ull;
   A.nstages = 0;  // set by stream_prepare from the device's shared memory
   int grid = 0;
   cudaError_t e = stream_prepare(A, m->n_sm, &grid);
@@ -731,6 +739,13 @@ int rv_load_model(const rv_config *cfg, const void *const *weights, void *stream
     return fail(RV_EINVAL, "unsupported configuration (d_model %% 32, ffn %% 16, head_dim 64/128, H/Hkv <= 8)");
   if ((long)c.max_batch * c.max_seq > (1L << 31) || c.max_batch > 4096)
     return fail(RV_EINVAL, "max_batch x max_seq too large");
+  {
+    // the batch-1 GEMV keeps element offsets of a matrix in 32 bits
+    const uint64_t qkv = (uint64_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+    const uint64_t big = std::max({(uint64_t)c.vocab, qkv, 2 * (uint64_t)c.ffn}) * (uint64_t)c.d_model;
+    if (big > 0xFFFFFFFFull || (uint64_t)c.d_model * c.ffn > 0xFFFFFFFFull)
+      return fail(RV_EINVAL, "a weight matrix above 2^32 - 1 elements");
+  }
   const int nw = 3 + 9 * c.n_layers;
   for (int i = 0; i < nw; ++i)
     if (!weights[i] && !(i == 2 && c.tied_embed)) return fail(RV_EINVAL, "weight %d is NULL", i);
@@ -1027,6 +1042,13 @@ int rv_set_option(rv_model *m, int option, int value) {
     m->quantizer = value;  // used by the next rv_quantize_river
     return RV_OK;
   }
+  if (option == RV_OPT_WAIT_LIMIT_US) {
+    if (value < 0) return fail(RV_EINVAL, "wait limit must be >= 0");
+    RV_CK(cudaStreamSynchronize(m->stream));
+    m->wait_us = value;
+    m->sargs.wait_ns = (unsigned long long)value * 1000ull;
+    return RV_OK;
+  }
   if (option != RV_OPT_DECODE_ENGINE) return fail(RV_EINVAL, "unknown option %d", option);
   if (value != RV_ENGINE_CHAIN && value != RV_ENGINE_PERSISTENT) return fail(RV_EINVAL, "unknown engine %d", value);
   if (value == RV_ENGINE_PERSISTENT && !m->stream_ready)
@@ -1125,6 +1147,11 @@ int rv_time_kernel(rv_model *m, int kind, int layer, int river, int iters, float
 }
 
 size_t rv_kv_bytes(const rv_model *m) { return m ? m->kv_bytes : 0; }
+
+int rv_debug_fail_alloc(int after) {
+  g_fail_after.store(after < 0 ? -1 : after);
+  return RV_OK;
+}
 
 int rv_offload_backbone(rv_model *m, int keep_layers) {
   g_err.clear();

@@ -45,6 +45,13 @@ extern "C" int rv_greedy_head_noalloc(const void *d_lm_head, const void *d_final
   if (vocab < 4 || vocab % 4) return fail(RV_EINVAL, "vocab must be a positive multiple of 4");
   if (d_model < 8 || d_model % 8) return fail(RV_EINVAL, "d_model must be a positive multiple of 8");
   if (d_model > 16384) return fail(RV_EINVAL, "d_model above the maximum of 16384 (shared-memory staging)");
+  // the GEMV keeps element offsets of the matrix in 32 bits
+  if ((uint64_t)vocab * (uint64_t)d_model > 0xFFFFFFFFull)
+    return fail(RV_EINVAL, "vocab x d_model above 2^32 - 1 elements");
+  // the kernel reads these with 16-byte loads and copies
+  if ((reinterpret_cast<uintptr_t>(d_lm_head) | reinterpret_cast<uintptr_t>(d_final_norm) |
+       reinterpret_cast<uintptr_t>(d_h)) & 15u)
+    return fail(RV_EINVAL, "d_lm_head, d_final_norm and d_h must be 16-byte aligned");
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(RV_ECUDA, "no usable device");
   unsigned char *base;

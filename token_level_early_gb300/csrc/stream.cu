@@ -173,6 +173,7 @@ struct Shared {
   volatile int *abort_flag;
   volatile int *issued;         // [nstages]: the last item issued into each stage
   int *misc;                    // [0] am-last flag
+  unsigned long long wait_ns;   // limit of a bounded wait
 };
 
 __device__ __forceinline__ bool aborted(const Shared &sh) { return *sh.abort_flag != 0; }
@@ -187,9 +188,9 @@ __device__ __forceinline__ unsigned long long gtime() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s: far beyond any healthy step
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s: far beyond any healthy step (the drain's limit)
 
-// Bounded wait on a stage barrier; false on timeout (after kWaitNs) or abort.
+// Bounded wait on a stage barrier; false on timeout (after sh.wait_ns) or abort.
 // try_wait itself suspends the thread for a while, so the loop spins
 // without sleeping (a sleep would add its wake-up latency to every item).
 __device__ __forceinline__ bool wait_stage(const Shared &sh, uint64_t *b, uint32_t ph, int32_t *err) {
@@ -198,7 +199,7 @@ __device__ __forceinline__ bool wait_stage(const Shared &sh, uint64_t *b, uint32
   for (uint32_t i = 1;; ++i) {
     if (mbar_try(b, ph)) return true;
     if (aborted(sh)) return false;
-    if ((i & 63) == 0 && gtime() - t0 > kWaitNs) break;
+    if ((i & 63) == 0 && gtime() - t0 > sh.wait_ns) break;
   }
   set_abort(sh, err, 32);
   return false;
@@ -217,7 +218,7 @@ __device__ __forceinline__ bool wait_item(const Shared &sh, int n, int NS, int32
     const unsigned long long t0 = gtime();
     for (uint32_t i = 1; sh.issued[slot] != n; ++i) {
       if (aborted(sh)) return false;
-      if ((i & 255) == 0 && gtime() - t0 > kWaitNs) {
+      if ((i & 255) == 0 && gtime() - t0 > sh.wait_ns) {
         set_abort(sh, err, 32);
         return false;
       }
@@ -228,7 +229,7 @@ __device__ __forceinline__ bool wait_item(const Shared &sh, int n, int NS, int32
 
 // Grid barrier of the compute warps: a counter that only grows within a
 // launch; thread 0 adds 1 (release) and polls (acquire) until epoch x blocks
-// have arrived.  Bounded: gives up (error bit 8, abort) after kWaitNs.
+// have arrived.  Bounded: gives up (error bit 8, abort) after sh.wait_ns.
 __device__ __forceinline__ void grid_barrier(const Shared &sh, unsigned *bar, unsigned &epoch, int32_t *err) {
   cbar();  // the block's writes are ordered before thread 0's release (cumulative)
   if (threadIdx.x == 0) {
@@ -238,7 +239,7 @@ __device__ __forceinline__ void grid_barrier(const Shared &sh, unsigned *bar, un
     if (!aborted(sh)) {
       const unsigned long long t0 = gtime();
       while ((int)(ld_acquire(bar) - target) < 0) {
-        if (gtime() - t0 > kWaitNs) {
+        if (gtime() - t0 > sh.wait_ns) {
           set_abort(sh, err, 8);
           break;
         }
@@ -325,7 +326,7 @@ __device__ void producer(const StreamArgs &A, const Shared &sh, int bid, int nb)
     {
       const unsigned long long t0 = gtime();
       while (*sh.known <= l) {
-        if (aborted(sh) || gtime() - t0 > kWaitNs) {
+        if (aborted(sh) || gtime() - t0 > sh.wait_ns) {
           if (!aborted(sh)) set_abort(sh, A.st.err, 32);
           stop = true;
           break;
@@ -940,6 +941,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
   sh.misc = ip + 2;
   sh.issued = ip + 4;
   sh.routes = ip + 4 + NS;
+  sh.wait_ns = A.wait_ns ? A.wait_ns : kWaitNs;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, bid = blockIdx.x, nb = gridDim.x;
   const int L = A.L;
@@ -1174,7 +1176,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode_stream(StreamArgs A) {
     A.st.next_ids[0] = ib == 0x7fffffff ? 0 : ib;
     A.st.route[0] = route;
     A.st.exit_layer[0] = exit_l;
-    A.st.len[0] = pos + 1;
+    // a step whose waits ran out did not happen: the position stays (its
+    // K/V slot is rewritten by the next step)
+    if ((*(volatile int32_t *)A.st.err & (8 | 32)) == 0) A.st.len[0] = pos + 1;
     A.bar[1] = 0u;
   }
 }

@@ -56,6 +56,7 @@ struct StreamArgs {
   float *dbg_h, *dbg_s, *dbg_logits;
   int nstages;        // ring stages
   int xbytes;         // activation / attention-tile region of shared memory
+  unsigned long long wait_ns;  // limit of every bounded wait (the final drain excepted)
 };
 
 // Work of one GEMV phase for one block: row groups [j0, j1) of the matrix,
