@@ -10,7 +10,7 @@ prompt, tau = 0.90; the Llama-3.2-1B-shaped workload is reported beside it.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload llama8b|llama1b|layer8b] [--modes tau,forced,full,river]
                   [--engine chain|persistent] [--no-cpu-baseline] [--no-secondary]
-                  [--no-fidelity]
+                  [--no-fidelity] [--no-extra]
 
 value : decode tokens/s, device-timed with CUDA events on the model's stream;
         tokens chained on the device (step i+1 consumes step i's id).
@@ -18,9 +18,13 @@ e2e   : the same metric through rv_decode_step with host buffers (token H2D,
         id + exit layer D2H inside the timed region), wall clock.
 Also in the line: every mode of the decode step (tau rule, forced exits,
 full backbone, all river) with its achieved GB/s, the river vs backbone layer
-time (layer_us), the roofline line of the dominant GEMV, single-kernel
-timings, backbone offloading (layers 1..3 kept), fidelity of the RTN and HQQ
-rivers against the full backbone, the CPU oracle baseline and the 1B shape.
+time (layer_us), the roofline line of the dominant kernel of the tau step
+(the river's gate/up GEMV; the backbone's beside it), single-kernel timings
+(GEMVs, LM head, decode attention), backbone offloading (layers 1..3 kept),
+fidelity of the RTN and HQQ rivers against the full backbone, the CPU oracle
+baseline, the 1B shape with its tau sweep (0.85, 0.90, 0.95), the batch-64
+mixed-exit workload and the 64K-context workload (KV bytes, decode rate,
+the decode attention's K/V read rate).
 Multi-GPU: independent replicas (the batch-1 decode step does not shard).
 """
 from __future__ import annotations
@@ -145,9 +149,10 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def profile_traffic():
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, when it was taken on the current kernel source; else None."""
+def profile_traffic(path):
+    """Per-launch DRAM bytes of the gate/up GEMV (path "int4" or "bf16") from
+    the committed ncu summary, when it was taken on the current kernel
+    source; else None."""
     if not os.path.exists(PROFILE_SUMMARY):
         return None
     vals = {}
@@ -160,7 +165,7 @@ def profile_traffic():
     if vals.get("kernel_source_sha256") != kernel_hash():
         return None
     try:
-        return float(vals["traffic_bytes_per_launch"])
+        return float(vals[f"traffic_bytes_per_launch_{path}"])
     except (KeyError, ValueError):
         return None
 
@@ -183,7 +188,7 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
     w = synth.make_weights(shape)
     log(f"[{wl_name}] weights generated in {time.time() - t0:.1f}s")
     prompt = synth.make_prompt(shape.vocab, 1, wl.prompt_len)
-    max_seq = wl.prompt_len + (len(MODES) + 2) * (warmup + steps) + steps + 72  # + room for the CPU baseline
+    max_seq = wl.prompt_len + (len(MODES) + 2 + len(wl.taus)) * (warmup + steps) + steps + 72  # + CPU baseline
     stream = torch.cuda.Stream()
     t0 = time.time()
     m = rv.Model(shape, w, 1, max_seq, stream=stream.cuda_stream)
@@ -194,7 +199,7 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
     first, e_seq = m.prefill(prompt, wl.prefill_tau)
     log(f"[{wl_name}] prefill {wl.prompt_len} tokens in {time.time() - t0:.1f}s, exit layer {int(e_seq[0])}")
 
-    n_ids = (len(MODES) + 2) * (warmup + steps) + 1
+    n_ids = (len(MODES) + 2 + len(wl.taus)) * (warmup + steps) + 1
     d_ids = torch.zeros(n_ids, dtype=torch.int32, device="cuda")
     d_exit = torch.zeros_like(d_ids)
     d_forced = torch.from_numpy(np.concatenate([synth.forced_exits(i, 1, L) for i in range(warmup + steps)])).cuda()
@@ -204,7 +209,7 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
     torch.cuda.synchronize()
     pos = [0]
 
-    def run_mode(mode, n, sampler=None):
+    def run_mode(mode, n, sampler=None, tau=tau):
         i0 = pos[0]
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
@@ -237,6 +242,17 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
         if clocks is not None:
             results[mode]["clocks"] = clocks
 
+    # the workload's tau sweep (the tau-rule step at every tau it names)
+    sweep = {}
+    if "tau" in modes and len(wl.taus) > 1:
+        for t_ in wl.taus:
+            run_mode("tau", warmup, tau=t_)
+            ctx0 = wl.prompt_len + pos[0]
+            ms, exits, _ = run_mode("tau", steps, tau=t_)
+            by = sum(token_bytes(shape, wl.group, e, ctx0 + i) for i, e in enumerate(exits))
+            sweep[f"{t_:.2f}"] = {"tokens_per_s": steps / (ms / 1e3), "achieved_gbs": by / (ms / 1e3) / 1e9,
+                                  "mean_exit_layer": float(np.mean(exits))}
+
     # the headline mode again on the other batch-1 engine, for comparison
     other = rv.ENGINE_PERSISTENT if engine == rv.ENGINE_CHAIN else rv.ENGINE_CHAIN
     m.set_engine(other)
@@ -256,7 +272,7 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
     kern = {}
     for name, kind, river in (("gateup_bf16", rv.TIME_GATEUP, False), ("gateup_int4", rv.TIME_GATEUP, True),
                               ("o_bf16", rv.TIME_O, False), ("o_int4", rv.TIME_O, True),
-                              ("lmhead_bf16", rv.TIME_LMHEAD, False)):
+                              ("lmhead_bf16", rv.TIME_LMHEAD, False), ("attention", rv.TIME_ATTN, False)):
         ms, by = m.time_kernel(kind, 1, river, 20)
         kern[name] = {"ms": ms, "bytes": by, "gbs": by / (ms / 1e3) / 1e9}
 
@@ -283,7 +299,124 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
             f"{offload['tau_tokens_per_s']:.1f} tokens/s")
     m.close()
     return {"modes": results, "e2e_tokens_per_s": steps / e2e_s, "kernels": kern, "cpu": cpu,
-            "prefill_exit": int(e_seq[0]), "offload": offload}
+            "prefill_exit": int(e_seq[0]), "offload": offload, "tau_sweep": sweep or None}
+
+
+def run_batch64(steps, warmup, dev_index, log):
+    """The batched heterogeneous-exit workload: 64 sequences of the 1B shape,
+    256-token prompts, per-row per-step forced exit layers (every layer of a
+    step mixes backbone and river rows writing the one cache).  Decode steps
+    through the device-pointer API, tokens chained on the device."""
+    import torch
+    import token_level_early_gb300 as rv
+
+    wl = synth.WORKLOADS["batch64"]
+    shape, B = wl.shape, wl.batch
+    L = shape.n_layers
+    torch.cuda.set_device(dev_index)
+    w = synth.make_weights(shape)
+    stream = torch.cuda.Stream()
+    T = wl.prompt_len + warmup + steps + 4
+    m = rv.Model(shape, w, B, T, stream=stream.cuda_stream)
+    m.quantize_river(wl.group, 1)
+    prompts = synth.make_prompt(shape.vocab, B, wl.prompt_len)
+    t0 = time.time()
+    first, _ = m.prefill(prompts, wl.prefill_tau)
+    log(f"[batch64] prefill {B} x {wl.prompt_len} tokens in {time.time() - t0:.1f}s")
+    ids = torch.zeros((warmup + steps + 1, B), dtype=torch.int32, device="cuda")
+    ex = torch.zeros_like(ids)
+    ids[0] = torch.from_numpy(first).cuda()
+    forced = torch.from_numpy(np.stack([synth.forced_exits(i, B, L) for i in range(warmup + steps)])).cuda()
+    torch.cuda.synchronize()
+
+    def run(i0, n):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(i0, i0 + n):
+            m.decode_step_dev(ids[i].data_ptr(), B, 0.9, forced[i].data_ptr(), ids[i + 1].data_ptr(),
+                              ex[i + 1].data_ptr())
+        ev1.record(stream)
+        ev1.synchronize()
+        m.sync_status()
+        return ev0.elapsed_time(ev1)
+
+    run(0, warmup)
+    ms = run(warmup, steps)
+    ex_np = ex[warmup + 1:].cpu().numpy()
+    m.close()
+    bb, rv_ = layer_bytes(shape, wl.group)
+    # both weight sets of every layer a step touches (a layer with rows on both
+    # paths streams both), the LM head, and the K/V of every row
+    layers_both = [(int((e < l + 1).any()), int((e >= l + 1).any())) for e in ex_np for l in range(L)]
+    wbytes = sum(r * rv_ + b * bb for b, r in layers_both) / steps + 2 * shape.vocab * shape.d_model
+    kv_pos = L * 2 * shape.n_kv_heads * shape.head_dim * 2
+    ctx = wl.prompt_len + warmup + steps / 2
+    by = wbytes + B * (ctx + 2) * kv_pos
+    out = {"workload": f"{shape.name} decode, batch {B}, {wl.prompt_len}-token prompts, per-row forced exits",
+           "tokens_per_s": B * steps / (ms / 1e3), "ms_per_step": ms / steps, "steps": steps,
+           "achieved_gbs": by / (ms / steps / 1e3) / 1e9, "bytes_per_step": by,
+           "mean_exit_layer": float(ex_np.mean())}
+    log(f"[batch64] {out['tokens_per_s']:.0f} tokens/s, {out['ms_per_step']:.2f} ms/step")
+    return out
+
+
+def run_long64k(steps, warmup, dev_index, log):
+    """The long-context workload: the 8B shape, a 65536-token prompt with the
+    sequence exit fixed at layer 20, then tau 0.90 decode steps; reports the
+    KV cache bytes (unchanged by building the river), the decode rate and the
+    decode attention's K/V read rate at this context."""
+    import torch
+    import token_level_early_gb300 as rv
+
+    wl = synth.WORKLOADS["long64k"]
+    shape = wl.shape
+    torch.cuda.set_device(dev_index)
+    w = synth.make_weights(shape)
+    stream = torch.cuda.Stream()
+    T = wl.prompt_len + warmup + steps + 4
+    m = rv.Model(shape, w, 1, T, stream=stream.cuda_stream)
+    del w
+    kv0 = m.kv_bytes()
+    m.quantize_river(wl.group, 1)
+    kv1 = m.kv_bytes()
+    prompt = synth.make_prompt(shape.vocab, 1, wl.prompt_len)
+    t0 = time.time()
+    first, e_seq = m.prefill(prompt, wl.prefill_tau, fixed_exit=wl.fixed_prefill_exit)
+    pre_s = time.time() - t0
+    log(f"[long64k] prefill {wl.prompt_len} tokens in {pre_s:.1f}s (exit layer {int(e_seq[0])})")
+    ids = torch.zeros(warmup + steps + 1, dtype=torch.int32, device="cuda")
+    ex = torch.zeros_like(ids)
+    ids[0] = int(first[0])
+    torch.cuda.synchronize()
+
+    def run(i0, n):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(i0, i0 + n):
+            m.decode_step_dev(ids[i:].data_ptr(), 1, wl.taus[0], None, ids[i + 1:].data_ptr(), ex[i + 1:].data_ptr())
+        ev1.record(stream)
+        ev1.synchronize()
+        m.sync_status()
+        return ev0.elapsed_time(ev1)
+
+    run(0, warmup)
+    ctx0 = wl.prompt_len + warmup
+    ms = run(warmup, steps)
+    exits = ex[warmup + 1:].cpu().numpy()
+    by = sum(token_bytes(shape, wl.group, e, ctx0 + i) for i, e in enumerate(exits))
+    a_ms, a_by = m.time_kernel(rv.TIME_ATTN, 1, False, 20)
+    m.close()
+    peak, _ = peak_hbm()
+    out = {"workload": f"{shape.name} decode, batch 1, {wl.prompt_len}-token prompt (sequence exit fixed at "
+                       f"layer {wl.fixed_prefill_exit}), tau {wl.taus[0]}",
+           "tokens_per_s": steps / (ms / 1e3), "ms_per_step": ms / steps, "steps": steps,
+           "achieved_gbs": by / (ms / 1e3) / 1e9, "mean_exit_layer": float(np.mean(exits)),
+           "kv_cache_bytes": kv0, "kv_cache_bytes_after_river": kv1, "prefill_s": pre_s,
+           "kv_read_bytes_per_step": 2 * shape.n_kv_heads * shape.head_dim * 2 * (ctx0 + steps // 2) * shape.n_layers,
+           "attention": {"layer": 1, "ms": a_ms, "bytes": a_by, "gbs": a_by / (a_ms / 1e3) / 1e9,
+                         "frac_of_measured_hbm": a_by / (a_ms / 1e3) / 1e9 / peak}}
+    log(f"[long64k] {out['tokens_per_s']:.1f} tokens/s; attention {out['attention']['gbs']:.0f} GB/s")
+    return out
 
 
 def cpu_baseline(gm, shape, w, wl, max_seq, tok, tau, log, budget_s=20.0):
@@ -462,6 +595,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-fidelity", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the batch-64 and 64K-context workloads")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local = env_rank()
@@ -517,21 +652,35 @@ def main():
         other = "llama1b" if args.workload == "llama8b" else "llama8b"
         r2 = run_workload(other, args.steps, args.warmup, local, False, rank0, log, MODES, args.engine)
         t2 = r2["modes"]["tau"]
-        sec = {"workload": other, "tokens_per_s": t2["tokens_per_s"], "achieved_gbs": t2["achieved_gbs"],
-               "mean_exit_layer": t2["mean_exit_layer"],
+        sec = {"workload": other, "tau": synth.WORKLOADS[other].taus[0], "tokens_per_s": t2["tokens_per_s"],
+               "achieved_gbs": t2["achieved_gbs"], "mean_exit_layer": t2["mean_exit_layer"],
+               "tau_sweep": r2.get("tau_sweep"),
                "forced_tokens_per_s": r2["modes"]["forced"]["tokens_per_s"],
                "full_backbone_tokens_per_s": r2["modes"]["full"]["tokens_per_s"],
                "all_river_tokens_per_s": r2["modes"]["river"]["tokens_per_s"],
                "e2e_tokens_per_s": r2["e2e_tokens_per_s"], "kernels": r2["kernels"]}
     fid = fidelity(args.workload, 32, local, log) if (rank0 and not args.no_fidelity) else None
+    extra = {}
+    if rank0 and world == 1 and not args.no_extra and args.workload == "llama8b":
+        extra["batch64"] = run_batch64(min(args.steps, 128), args.warmup, local, log)
+        extra["long64k"] = run_long64k(min(args.steps, 64), args.warmup, local, log)
     if not rank0:
         return
     peak, peak_kind = peak_hbm()
-    k = res["kernels"]["gateup_bf16"]
-    roof = {"bound": "hbm", "kernel": "k_gemv_b1<bf16, RMSNorm prologue, SwiGLU epilogue> (gate/up, layer 1)",
-            "achieved": k["gbs"], "peak": peak, "unit": "GB/s", "frac": k["gbs"] / peak,
-            "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-            "traffic": profile_traffic(), "bytes_per_launch": k["bytes"], "ms_per_launch": k["ms"]}
+
+    def roof_of(name, kernel, path):
+        k = res["kernels"][name]
+        return {"bound": "hbm", "kernel": kernel, "achieved": k["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": k["gbs"] / peak,
+                "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs), burst",
+                "traffic": profile_traffic(path), "bytes_per_launch": k["bytes"], "ms_per_launch": k["ms"]}
+
+    # the dominant kernel of the headline (tau) step is the river's gate/up:
+    # most of its layers run in the river
+    roof = roof_of("gateup_int4", "k_gemv_b1<int4 river weights, RMSNorm prologue, SwiGLU epilogue> "
+                                  "(gate/up, layer 1)", "int4")
+    roof_bb = roof_of("gateup_bf16", "k_gemv_b1<bf16, RMSNorm prologue, SwiGLU epilogue> (gate/up, layer 1)",
+                      "bf16")
     L = wl.shape.n_layers
     modes = {m_: {k_: v_ for k_, v_ in r.items() if k_ != "clocks"} for m_, r in res["modes"].items()}
     line = {"metric": METRIC, "value": world * 1e3 / ms, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -543,7 +692,11 @@ def main():
             "speedup_vs_full_backbone": (tau_r["tokens_per_s"] / res["modes"]["full"]["tokens_per_s"]
                                          if "full" in res["modes"] else None),
             "layer_us": layer_us(res, L),
-            "roofline": roof, "kernels": res["kernels"], "cpu_baseline": res["cpu"], "offload": res["offload"],
+            "roofline": roof, "roofline_backbone": roof_bb,
+            "step_roofline": {"achieved": tau_r["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                              "frac": tau_r["achieved_gbs"] / peak,
+                              "what": "algorithmic bytes of the whole tau step / its time"},
+            "kernels": res["kernels"], "cpu_baseline": res["cpu"], "offload": res["offload"],
             "fidelity": fid,
             "e2e": {"value": world * e2e, "unit": "tokens/s", "h2d_bytes_per_step": 4 * 6,
                     "d2h_bytes_per_step": 4 * 4},
@@ -553,6 +706,8 @@ def main():
             "dtype_detail": "bf16 weights/activations/KV, int4 river weights with fp16 scale/zero, fp32 accumulation"}
     if sec:
         line["secondary"] = sec
+    if extra:
+        line.update(extra)
     print(json.dumps(line), flush=True)
 
 

@@ -196,12 +196,15 @@ int rv_debug_fail_alloc(int after);
  * (CUDA events) and its algorithmic HBM bytes per launch in *bytes (weights,
  * the activation vector read, the outputs written).
  * kind: RV_TIME_GATEUP (RMSNorm + gate/up + SwiGLU of `layer`), RV_TIME_O
- * (O projection + residual), RV_TIME_LMHEAD (final norm + LM head + argmax).
- * river selects the int4 copy (gate/up, O).  Leaves the KV cache and the
- * cached positions untouched; the step's activation buffers are overwritten. */
+ * (O projection + residual), RV_TIME_LMHEAD (final norm + LM head + argmax),
+ * RV_TIME_ATTN (the decode attention of row 0 in `layer` at its current
+ * position; bytes = the K/V it reads).  river selects the int4 copy
+ * (gate/up, O).  Leaves the KV cache and the cached positions untouched;
+ * the step's activation buffers are overwritten. */
 #define RV_TIME_GATEUP 0
 #define RV_TIME_O 1
 #define RV_TIME_LMHEAD 2
+#define RV_TIME_ATTN 3
 int rv_time_kernel(rv_model *m, int kind, int layer, int river, int iters, float *ms_per_launch, double *bytes);
 
 /* Greedy LM head without allocation: final RMSNorm (gain d_final_norm, eps

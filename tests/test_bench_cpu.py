@@ -51,8 +51,10 @@ def test_layer_us(bench):
 
 def test_profile_traffic_follows_kernel_hash(bench, tmp_path, monkeypatch):
     f = tmp_path / "p.md"
-    f.write_text(f"- kernel_source_sha256: {bench.kernel_hash()}\n- traffic_bytes_per_launch: 123\n")
+    f.write_text(f"- kernel_source_sha256: {bench.kernel_hash()}\n- traffic_bytes_per_launch_int4: 123\n"
+                 "- traffic_bytes_per_launch_bf16: 456\n")
     monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(f))
-    assert bench.profile_traffic() == 123.0
-    f.write_text("- kernel_source_sha256: 0000000000000000\n- traffic_bytes_per_launch: 123\n")
-    assert bench.profile_traffic() is None
+    assert bench.profile_traffic("int4") == 123.0
+    assert bench.profile_traffic("bf16") == 456.0
+    f.write_text("- kernel_source_sha256: 0000000000000000\n- traffic_bytes_per_launch_int4: 123\n")
+    assert bench.profile_traffic("int4") is None

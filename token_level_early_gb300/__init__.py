@@ -33,7 +33,7 @@ EXPORTED = ("rv_last_error", "rv_load_model", "rv_quantize_river", "rv_export_ri
 OPT_DECODE_ENGINE, ENGINE_CHAIN, ENGINE_PERSISTENT = 0, 0, 1
 OPT_QUANTIZER, QUANT_RTN, QUANT_HQQ = 1, 0, 1
 OPT_WAIT_LIMIT_US = 2
-TIME_GATEUP, TIME_O, TIME_LMHEAD = 0, 1, 2
+TIME_GATEUP, TIME_O, TIME_LMHEAD, TIME_ATTN = 0, 1, 2, 3
 
 
 def nvcc() -> str:

@@ -1085,8 +1085,34 @@ int rv_debug_dump(rv_model *m, int what, void *dst, size_t bytes) {
 int rv_time_kernel(rv_model *m, int kind, int layer, int river, int iters, float *ms_per_launch, double *bytes) {
   g_err.clear();
   if (check_common(m)) return RV_EINVAL;
-  if (!ms_per_launch || !bytes || iters < 1 || kind < 0 || kind > 2) return fail(RV_EINVAL, "bad argument");
+  if (!ms_per_launch || !bytes || iters < 1 || kind < 0 || kind > 3) return fail(RV_EINVAL, "bad argument");
   if (layer < 1 || layer > m->L) return fail(RV_EINVAL, "layer out of range");
+  if (kind == RV_TIME_ATTN) {
+    // the decode attention of row 0 at its current position len: reads the
+    // K/V of positions 0..len of the layer (q and the output are the step's
+    // own buffers, whatever they hold)
+    cudaStream_t s = m->stream;
+    RV_CK(cudaStreamSynchronize(s));
+    AttnArgs at{};
+    at.kv = m->kv; at.layer = layer - 1; at.H = m->H; at.Hkv = m->Hkv; at.hd = m->hd; at.act = m->act;
+    at.q = m->qbuf; at.o = m->obuf; at.len = m->st.len; at.splits = m->attn_splits_b1;
+    at.part = m->attn_part; at.counter = m->attn_counter;
+    *bytes = 2.0 * m->Hkv * m->hd * 2.0 * (double)(m->h_len[0] + 1);
+    cudaEvent_t e0, e1;
+    RV_CK(cudaEventCreate(&e0));
+    RV_CK(cudaEventCreate(&e1));
+    RV_CK(launch_attn_decode(at, 1, s));  // warm launch
+    RV_CK(cudaEventRecord(e0, s));
+    for (int i = 0; i < iters; ++i) RV_CK(launch_attn_decode(at, 1, s));
+    RV_CK(cudaEventRecord(e1, s));
+    RV_CK(cudaEventSynchronize(e1));
+    float ms = 0.f;
+    RV_CK(cudaEventElapsedTime(&ms, e0, e1));
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    *ms_per_launch = ms / iters;
+    return RV_OK;
+  }
   if (river && (!m->has_river || kind == RV_TIME_LMHEAD)) return fail(RV_ESTATE, "no river copy for this kernel");
   if (!river && kind != RV_TIME_LMHEAD && layer > m->cap) return fail(RV_ESTATE, "backbone layer %d is offloaded", layer);
   cudaStream_t s = m->stream;
