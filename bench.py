@@ -10,7 +10,7 @@ prompt, tau = 0.90; the Llama-3.2-1B-shaped workload is reported beside it.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload llama8b|llama1b|layer8b] [--modes tau,forced,full,river]
                   [--engine chain|persistent] [--no-cpu-baseline] [--no-secondary]
-                  [--no-fidelity] [--no-extra]
+                  [--no-fidelity] [--no-extra] [--only batch64|long64k]
 
 value : decode tokens/s, device-timed with CUDA events on the model's stream;
         tokens chained on the device (step i+1 consumes step i's id).
@@ -597,6 +597,8 @@ def main():
     ap.add_argument("--no-fidelity", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the batch-64 and 64K-context workloads")
+    ap.add_argument("--only", choices=["batch64", "long64k"],
+                    help="time only this workload (its own JSON line; for profiling commands)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local = env_rank()
@@ -639,6 +641,16 @@ def main():
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     rv.lib()
+    if args.only:
+        if not rank0 or world > 1:
+            return
+        fn = run_batch64 if args.only == "batch64" else run_long64k
+        r = fn(args.steps, args.warmup, local, log)
+        print(json.dumps({"metric": METRIC, "value": r["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                          "data": "synthetic", "config": {"workload": r["workload"]}, args.only: r}), flush=True)
+        return
     modes = tuple(x for x in args.modes.split(",") if x in MODES) or MODES
     res = run_workload(args.workload, args.steps, args.warmup, local, not args.no_cpu_baseline, rank0, log, modes,
                        args.engine, want_offload="tau" in modes)

@@ -151,7 +151,12 @@ def test_tiny_prefill_tau_rule_batched(weights):
 
 def test_ongrid_river_matches_backbone_on_gpu():
     """On-grid weights: the int4 river equals the backbone, so the all-river
-    and all-backbone GPU paths give the same logits (fp32 rounding aside)."""
+    and all-backbone GPU paths give the same logits up to fp32 rounding.  The
+    two paths sum the same products in different orders (the int4 path folds
+    the zero point per run), so a 16-bit activation occasionally rounds the
+    other way (fp16 half-ulp 2^-11 relative), which moves the logits by about
+    1e-3; a wrong weight (one int4 step is 1/15 of a group's range) moves them
+    by orders of magnitude more.  Bound: 5e-3."""
     ws, _ = ongrid_weights(TINY, 64, seed=4)
     gm = rv.Model(TINY, ws, 1, 16)
     gm.quantize_river(64)
@@ -163,7 +168,7 @@ def test_ongrid_river_matches_backbone_on_gpu():
         gm.prefill(prompt, 2.0, fixed_exit=e)
         gm.decode_step([5], 2.0, np.array([e], dtype=np.int32))
         out.append(gm.dump(rv.DUMP_LOGITS)[0].copy())
-    assert np.abs(out[0] - out[1]).max() < 1e-3
+    assert np.abs(out[0] - out[1]).max() < 5e-3
     gm.close()
 
 

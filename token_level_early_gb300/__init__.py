@@ -20,7 +20,7 @@ _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "librv.so")
 _CSRC = os.path.join(_HERE, "csrc")
 _BUILD = os.path.join(_ROOT, "_build")
-SOURCES = ["api.cu", "decode_b1.cu", "attention.cu", "general.cu", "quant.cu", "noalloc.cu", "stream.cu", "gemm_tc.cu"]
+SOURCES = ["api.cu", "decode_b1.cu", "attention.cu", "general.cu", "quant.cu", "noalloc.cu", "stream.cu", "gemm_tc.cu", "rows_mma.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 RV_OK, RV_EINVAL, RV_ENOMEM, RV_ECUDA, RV_ECAPACITY, RV_ESTATE, RV_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6

@@ -103,9 +103,10 @@ struct rv_model {
   float *partials = nullptr;
   unsigned *seq_min = nullptr;  // [Bmax] prefill sequence-exit minima (order-preserving encoding)
   unsigned *counters = nullptr;
-  int attn_splits_b1 = 1, attn_splits_max = 1, attn_cluster = 1;
+  int attn_splits_max = 1, attn_cluster = 1;
   float *attn_part = nullptr;
   unsigned *attn_counter = nullptr;
+  unsigned long long *head_keys = nullptr;  // [Bmax] greedy-pick keys of the batched LM head (zero between steps)
 
   // general-path workspace (grown on demand)
   long ws_rows = 0;
@@ -237,6 +238,20 @@ Mat make_mat(const rv_model *m, const LayerDev &ly, int which) {
 // per SM (the launcher also caps the grid at one resident wave).
 int gemv_grid(const rv_model *m, int) { return 4 * m->n_sm; }
 
+// Decode-attention plan for rows 0..B-1 at their current positions (the
+// captured step of batch B is keyed by it).
+int attn_plan(const rv_model *m, int B, AttnArgs *at) {
+  int pmax = 0;
+  for (int b = 0; b < B && b < (int)m->h_len.size(); ++b) pmax = m->h_len[b] > pmax ? m->h_len[b] : pmax;
+  int splits = 1;
+  const int gm = attn_dec_plan(B, m->Hkv, m->n_sm, m->attn_cluster, m->attn_splits_max, pmax, &splits);
+  if (at) {
+    at->global_merge = gm;
+    at->splits = splits;
+  }
+  return gm;
+}
+
 // -------------------------------------------------------------- batch-1 step
 
 int enqueue_step_b1(rv_model *m, cudaStream_t s) {
@@ -273,8 +288,9 @@ int enqueue_step_b1(rv_model *m, cudaStream_t s) {
 
     AttnArgs at{};
     at.kv = m->kv; at.layer = l; at.H = m->H; at.Hkv = m->Hkv; at.hd = m->hd; at.act = m->act;
-    at.q = m->qbuf; at.o = m->obuf; at.len = m->st.len; at.splits = m->attn_splits_b1;
+    at.q = m->qbuf; at.o = m->obuf; at.len = m->st.len;
     at.part = m->attn_part; at.counter = m->attn_counter;
+    attn_plan(m, 1, &at);
     RV_CK(launch_attn_decode(at, 1, s, 1));
 
     // O projection + residual
@@ -317,20 +333,29 @@ int enqueue_step_b1(rv_model *m, cudaStream_t s) {
 
 // -------------------------------------------------------------- general path
 
-// Rows GEMM: the tensor-core kernel for 16-bit matrices where the device has
-// it, the CUDA-core kernel for the int4 river copies.
-// River rows take the tensor-core path (the matrix split into exact 16-bit
-// hi + lo, two GEMMs) from this many rows up; below it the int4 CUDA-core
-// GEMM reads fewer bytes.
+// Rows GEMM: the tcgen05 kernel for 16-bit matrices where the device has it;
+// river copies: fewer than 256 rows on the tensor pipe straight from the int4
+// codes, more through the matrix's 16-bit hi + lo copies on tcgen05.
+// River rows take the tcgen05 path (the matrix split into exact 16-bit hi +
+// lo, two GEMMs) from this many rows up; below it the int4 kernel, which
+// reads a quarter of the bytes of either 16-bit copy, is the faster one.
 constexpr long kRiverTcRows = 256;
+constexpr int kRowsMmaMax16 = 64;
 
 static cudaError_t gemm_rows(rv_model *m, const Mat &mt, int river, const float *X, float *Y, const int32_t *list,
                              const int32_t *count, int max_rows, cudaStream_t s) {
+  // up to 64 rows of a 16-bit matrix: the mma.sync rows kernel splits K over
+  // clusters, where the tcgen05 GEMM would run one 128-row tile per 128
+  // columns of N and leave most SMs idle
+  if (!river && max_rows <= kRowsMmaMax16 && rows_b16_supported(mt))
+    return launch_rows_b16(mt, m->act, X, Y, list, count, max_rows, m->n_sm, s);
   if (m->tc_gemm && mt.K % 8 == 0 && max_rows <= m->ws_rows) {
     if (!river) return launch_gemm_tc(mt, m->act, X, Y, list, count, max_rows, m->gXb, m->st.err, s);
     if (max_rows >= kRiverTcRows && m->gWhi)
       return launch_gemm_tc_river(mt, m->act, X, Y, list, count, max_rows, m->gXb, m->gWhi, m->gWlo, m->st.err, s);
   }
+  if (river && max_rows < kRiverTcRows && rows_i4_supported(mt))
+    return launch_rows_i4(mt, m->act, X, Y, list, count, max_rows, m->n_sm, s);
   return launch_gemm_rows(mt, river, m->act, X, Y, list, count, max_rows, s);
 }
 
@@ -394,12 +419,9 @@ int enqueue_layer_rows(rv_model *m, int l, int B, int T, const int32_t *base, cu
   if (T == 1) {
     AttnArgs at{};
     at.kv = m->kv; at.layer = l; at.H = m->H; at.Hkv = m->Hkv; at.hd = m->hd; at.act = act;
-    at.q = m->gQ; at.o = m->gO; at.len = base; at.splits = m->attn_splits_max;
+    at.q = m->gQ; at.o = m->gO; at.len = base;
     at.part = m->attn_part; at.counter = m->attn_counter;
-    // decode rows: cluster size (a power of two) sized for the batch
-    int sp = 1;
-    while (2 * sp <= m->attn_cluster && 2 * sp * m->Hkv * B <= 2 * m->n_sm) sp *= 2;
-    at.splits = sp;
+    attn_plan(m, B, &at);
     RV_CK(launch_attn_decode(at, B, s));
   } else {
     AttnRowsArgs ar{};
@@ -426,8 +448,14 @@ int enqueue_head_rows(rv_model *m, int B, int bump_len, int set_len, cudaStream_
   RV_CK(launch_rmsnorm_rows(m->gHf, m->final_norm, m->d, m->c.rms_eps, m->act, m->gXf, nullptr, m->d_nrows, B, s));
   Mat lm{};
   lm.w = m->lm_head; lm.N = m->V; lm.K = m->d;
-  RV_CK(gemm_rows(m, lm, 0, m->gXf, m->gLogits, nullptr, m->d_nrows, B, s));
-  RV_CK(launch_argmax_rows(m->gLogits, m->V, B, m->st, bump_len, set_len, s));
+  if (B <= kRowsMmaMax16 && rows_b16_supported(lm)) {
+    // the greedy pick rides on the LM-head kernel (one key per row)
+    RV_CK(launch_rows_b16(lm, m->act, m->gXf, m->gLogits, nullptr, m->d_nrows, B, m->n_sm, s, m->head_keys));
+    RV_CK(launch_pick_finish(m->head_keys, B, m->st, bump_len, set_len, s));
+  } else {
+    RV_CK(gemm_rows(m, lm, 0, m->gXf, m->gLogits, nullptr, m->d_nrows, B, s));
+    RV_CK(launch_argmax_rows(m->gLogits, m->V, B, m->st, bump_len, set_len, s));
+  }
   if (m->debug)
     RV_CK(cudaMemcpyAsync(m->dbg_logits, m->gLogits, sizeof(float) * B * m->V, cudaMemcpyDeviceToDevice, s));
   return RV_OK;
@@ -540,7 +568,8 @@ int launch_step(rv_model *m, int B) {
     RV_CK(stream_launch(m->sargs, m->stream_grid, m->stream));
     return RV_OK;
   }
-  auto it = m->graphs.find(B);
+  const int key = 2 * B + attn_plan(m, B, nullptr);
+  auto it = m->graphs.find(key);
   if (it == m->graphs.end()) {
     if (B > 1) {
       int rc = ensure_ws(m, m->Bmax);
@@ -559,7 +588,7 @@ int launch_step(rv_model *m, int B) {
     cudaError_t ei = cudaGraphInstantiate(&ge, g, 0);
     cudaGraphDestroy(g);
     if (ei != cudaSuccess) return fail(RV_ECUDA, "graph instantiate failed: %s", cudaGetErrorString(ei));
-    it = m->graphs.emplace(B, ge).first;
+    it = m->graphs.emplace(key, ge).first;
   }
   RV_CK(cudaGraphLaunch(it->second, m->stream));
   return RV_OK;
@@ -705,15 +734,16 @@ static int load_impl(rv_model *m, const rv_config *cfg, const void *const *weigh
   int sp = (2 * m->n_sm + m->Hkv - 1) / m->Hkv;
   const int tiles = (m->Tmax + 31) / 32;
   if (sp > tiles) sp = tiles;
-  if (sp > 128) sp = 128;
+  if (sp > kAttnMaxSplits) sp = kAttnMaxSplits;
   if (sp < 1) sp = 1;
   m->attn_splits_max = sp;  // split count of the persistent kernel's attention
   // decode attention: one cluster of splits per (row, kv head)
   m->attn_cluster = attn_dec_max_cluster(m->hd, m->H / m->Hkv, m->act);
   if (m->attn_cluster < 1) return fail(RV_ECUDA, "decode attention cannot be launched on this device");
-  m->attn_splits_b1 = m->attn_cluster;
   RV_ALLOC(A, m->attn_part, sizeof(float) * (size_t)m->Bmax * m->H * sp * (m->hd + 2));
   RV_ALLOC(A, m->attn_counter, sizeof(unsigned) * (size_t)m->Bmax * m->Hkv);
+  RV_ALLOC(A, m->head_keys, sizeof(unsigned long long) * (size_t)m->Bmax);
+  RV_CK(cudaMemsetAsync(m->head_keys, 0, sizeof(unsigned long long) * (size_t)m->Bmax, m->stream));
   RV_CK(cudaMemsetAsync(m->attn_counter, 0, sizeof(unsigned) * (size_t)m->Bmax * m->Hkv, m->stream));
   // head rows for the general path, identity list
   RV_ALLOC(A, m->gHf, sizeof(float) * (size_t)m->Bmax * d);
@@ -1095,8 +1125,9 @@ int rv_time_kernel(rv_model *m, int kind, int layer, int river, int iters, float
     RV_CK(cudaStreamSynchronize(s));
     AttnArgs at{};
     at.kv = m->kv; at.layer = layer - 1; at.H = m->H; at.Hkv = m->Hkv; at.hd = m->hd; at.act = m->act;
-    at.q = m->qbuf; at.o = m->obuf; at.len = m->st.len; at.splits = m->attn_splits_b1;
+    at.q = m->qbuf; at.o = m->obuf; at.len = m->st.len;
     at.part = m->attn_part; at.counter = m->attn_counter;
+    attn_plan(m, 1, &at);
     *bytes = 2.0 * m->Hkv * m->hd * 2.0 * (double)(m->h_len[0] + 1);
     cudaEvent_t e0, e1;
     RV_CK(cudaEventCreate(&e0));

@@ -11,12 +11,12 @@
 // aitrends.kr KV Share).
 //
 // Decode rows use k_attn_dec: the splits of one (row, kv head) form a
-// thread-block cluster.  Each split streams its share of the past positions
-// 0..p-1 (final before the step starts) through a shared-memory ring that it
-// fills before the programmatic-dependent-launch wait; only q and the K/V of
-// position p come from the QKV kernel it follows.  A split whose tiles all
-// fit the ring takes its scores in one pass and one max/sum; longer ones use
-// the online softmax.  The splits merge their softmax states through
+// thread-block cluster.  Each split's warps stream its share of the past
+// positions 0..p-1 (final before the step starts) through private
+// shared-memory rings filled before the programmatic-dependent-launch wait,
+// and run S = q K^T and O += P V on the tensor pipe for all the kv head's
+// query heads at once; only q and the K/V of position p come from the QKV
+// kernel it follows.  The warps merge in shared memory, the splits through
 // distributed shared memory.
 #include <cooperative_groups.h>
 #include <math.h>
@@ -140,92 +140,106 @@ __global__ void __launch_bounds__(GRP * 32) k_attn(AttnArgs a, int T_per_row, co
   for (int r = 0; r < PER; ++r) a.o[orow + lane + 32 * r] = round_act(acc[r] * inv, a.act);
 }
 
-// ---- decode: clustered split-KV attention ----------------------------------
-constexpr int DTT = 32;   // positions per tile (one per lane in the score pass)
-constexpr int DNST = 5;   // ring stages: a split of up to DNST - 1 tiles is in flight before the wait
-
-template <int HD>
-struct DecTile {
-  static constexpr int KROW = HD * 2 + 16;  // padded K row: lane-per-row 16-byte reads hit distinct banks
-  static constexpr int VROW = HD * 2;
-  static constexpr int BYTES = DTT * (KROW + VROW);
-};
-
-template <int HD>
-static size_t dec_smem(int grp) {
-  return (size_t)DNST * DecTile<HD>::BYTES + sizeof(float) * grp * (HD + 2) + sizeof(float) * grp * DNST * DTT;
+// ---- tensor-pipe helpers (decode and prefill) ------------------------------
+__device__ __forceinline__ void cp16z(unsigned dst, const void *src, bool valid) {
+  const int n = valid ? 16 : 0;  // 0: zero-fill, nothing read
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
-
-// q . K[row] for one position: the lane's K row (16-bit, padded) against q as
-// 16-bit pairs, mixed-precision FMAs into four fp32 partial sums.
-template <int HD, int ACT>
-__device__ __forceinline__ float k_dot_q(const unsigned char *krow, const uint32_t *qr) {
-  const uint4 *kr = reinterpret_cast<const uint4 *>(krow);
-  float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-#pragma unroll
-  for (int j = 0; j < HD / 8; ++j) {
-    const uint4 k = kr[j];
-    d0 = fma_lo16<ACT>(k.x, qr[4 * j], d0);
-    d1 = fma_hi16<ACT>(k.x, qr[4 * j], d1);
-    d2 = fma_lo16<ACT>(k.y, qr[4 * j + 1], d2);
-    d3 = fma_hi16<ACT>(k.y, qr[4 * j + 1], d3);
-    d0 = fma_lo16<ACT>(k.z, qr[4 * j + 2], d0);
-    d1 = fma_hi16<ACT>(k.z, qr[4 * j + 2], d1);
-    d2 = fma_lo16<ACT>(k.w, qr[4 * j + 3], d2);
-    d3 = fma_hi16<ACT>(k.w, qr[4 * j + 3], d3);
-  }
-  return (d0 + d1) + (d2 + d3);
+__device__ __forceinline__ void ldsm_x4(uint32_t *r, unsigned addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
 }
-
-// o[r] += sum over the tile's first n positions t of p[t] * V[t][lane * PER + r],
-// p broadcast from shared memory (all lanes read the same word); full tiles
-// unrolled with two accumulator sets to halve the dependent FMA chains.
-template <int HD, int ACT>
-__device__ __forceinline__ void v_accumulate(const unsigned char *tv, const float *pw, int n, int lane, float *o) {
-  constexpr int PER = HD / 32, VROW = HD * 2;
-  if (n == DTT) {
-    float e[PER];
-#pragma unroll
-    for (int r = 0; r < PER; ++r) e[r] = 0.f;
-#pragma unroll
-    for (int t = 0; t < DTT; t += 2) {
-      const float p0 = pw[t], p1 = pw[t + 1];
-      const uint16_t *v0 = reinterpret_cast<const uint16_t *>(tv + t * VROW) + lane * PER;
-      const uint16_t *v1 = v0 + HD;
-#pragma unroll
-      for (int r = 0; r < PER; ++r) {
-        o[r] = fmaf(p0, act_to_f(v0[r], ACT), o[r]);
-        e[r] = fmaf(p1, act_to_f(v1[r], ACT), e[r]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < PER; ++r) o[r] += e[r];
-  } else {
-    for (int t = 0; t < n; ++t) {
-      const float pt = pw[t];
-      const uint16_t *vr = reinterpret_cast<const uint16_t *>(tv + t * VROW) + lane * PER;
-#pragma unroll
-      for (int r = 0; r < PER; ++r) o[r] = fmaf(pt, act_to_f(vr[r], ACT), o[r]);
-    }
-  }
+__device__ __forceinline__ void ldsm_x4_t(uint32_t *r, unsigned addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
 }
-
+template <int ACT>
+__device__ __forceinline__ void mma16816(float *d, const uint32_t *a, const uint32_t *b) {
+  if (ACT == 1)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
 __device__ __forceinline__ uint32_t pack_act2(float lo, float hi, int act) {
   return (uint32_t)f_to_act(lo, act) | ((uint32_t)f_to_act(hi, act) << 16);
 }
 
-template <int HD, int GRP, int ACT>
-__global__ void __launch_bounds__(GRP * 32, 1) k_attn_dec(AttnArgs a) {
+// ---- decode: split-KV attention on the tensor pipe -------------------------
+// Block (split sp, kv head g, row b) of DNW warps.  The split's tiles of 32
+// past positions are dealt round-robin to its warps; each warp streams its
+// own tiles through a private cp.async ring of NS slots (no block barrier in
+// the loop), the first ones issued before the programmatic-dependent-launch
+// wait.  Per tile, one warp serves all GRP query heads of the kv head:
+//   S = q K^T       m16n8k16, M = heads (rows >= GRP are zero), N = positions,
+//   O^T += V^T P^T  M = head dims, N = heads, K = positions,
+// so the score fragments are already the B fragments of the P V product (no
+// shuffle through shared memory).  Scores are kept in the log2 domain
+// (scaled by log2(e) / sqrt(hd)); P enters as two 16-bit terms hi + lo like
+// the prefill kernel.  After the loop the warps' softmax states and the
+// position p itself (its K/V come from the QKV kernel this kernel follows)
+// merge in shared memory, then the splits merge:
+//   short contexts (GM = false): the splits of a (row, kv head) form a
+//     thread-block cluster and merge through distributed shared memory; one
+//     ring slot per warp keeps a block small (several per SM, so clusters of
+//     16 find room and the neighbouring GEMV kernels keep theirs);
+//   long contexts (GM = true): no cluster, about one block per SM with a deep
+//     ring, the splits' states go through global memory and the last block of
+//     a (row, kv head) to finish merges them (an atomic ticket, no waiting).
+constexpr int DTT = 32;  // positions per tile
+constexpr int DNW = 4;   // warps per block
+
+template <int HD>
+struct DecTile {
+  static constexpr int ROW = HD * 2 + 16;           // padded row: the 8 rows of an ldmatrix hit distinct banks
+  static constexpr int BYTES = 2 * DTT * ROW;       // K rows then V rows
+  static constexpr int NS_LONG = HD == 64 ? 6 : 3;  // ring slots per warp, long contexts
+};
+
+// Merge-phase layout (floats, over the ring once it is drained):
+//   part [GRP][HD]       the block's O (read by the other splits)
+//   wpo  [DNW][GRP][HD]  the warps' O
+//   pm   [GRP][2]        the block's (max, sum) (read by the other splits)
+//   wml  [DNW][GRP][2]   the warps' (max, sum)
+//   sps  [GRP]           score of position p;  spv [HD] its V row
+//   gml  [splits][GRP][2] the splits' (max, sum), then the last-block flag (global merge)
+template <int HD>
+__host__ __device__ constexpr int dec_merge_floats(int grp) {
+  return (1 + DNW) * grp * HD + 2 * grp + DNW * grp * 2 + grp + HD + kAttnMaxSplits * grp * 2 + 1;
+}
+template <int HD, int NS>
+static size_t dec_smem(int grp) {
+  const size_t merge = sizeof(float) * (size_t)dec_merge_floats<HD>(grp);
+  const size_t ring = (size_t)DNW * NS * DecTile<HD>::BYTES;
+  return merge > ring ? merge : ring;
+}
+
+template <int HD, int GRP, int ACT, int NS, bool GM>
+__global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
   using TL = DecTile<HD>;
-  constexpr int NT = GRP * 32, PER = HD / 32, PR = HD / 8;
+  constexpr int KS = HD / 16, PR = HD / 8, PER = HD / 32;
+  constexpr int PF = NS > 1 ? NS - 1 : 1;  // tiles a warp has in flight before its first wait
+  static_assert(GRP <= 8, "one m16n8 tile holds at most 8 heads per kv head");
   extern __shared__ __align__(16) unsigned char sm[];
-  // per head: o [GRP][HD], then (running max, sum) [GRP][2]
-  float *part = reinterpret_cast<float *>(sm + DNST * TL::BYTES);
-  float *pbuf = part + GRP * (HD + 2);  // [GRP][DNST * DTT]: softmax numerators of the warp's positions
-  cg::cluster_group cl = cg::this_cluster();
-  const int cs = (int)cl.num_blocks(), sp = (int)cl.block_rank();
+  int cs, sp;
+  if (GM) {
+    cs = (int)gridDim.x;
+    sp = (int)blockIdx.x;
+  } else {
+    cg::cluster_group cl = cg::this_cluster();
+    cs = (int)cl.num_blocks();
+    sp = (int)cl.block_rank();
+  }
   const int g = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+  const bool last = sp == cs - 1;
 
   // The token sits at position p = len[b] (advanced by the previous step's
   // LM-head kernel, final here); positions < p were written by earlier steps.
@@ -233,202 +247,358 @@ __global__ void __launch_bounds__(GRP * 32, 1) k_attn_dec(AttnArgs a) {
   const int ntile = (p + DTT - 1) / DTT;
   const int per = (ntile + cs - 1) / cs;
   const int tb = min(ntile, sp * per), te = min(ntile, tb + per);
+  const int nmine = te - tb > warp ? (te - tb - warp + DNW - 1) / DNW : 0;  // tiles tb + warp + DNW * i
   const uint16_t *Kb = a.kv.base + a.kv.idx(a.layer, 0, b, g, 0);
   const uint16_t *Vb = a.kv.base + a.kv.idx(a.layer, 1, b, g, 0);
-  const unsigned sbase = (unsigned)__cvta_generic_to_shared(sm);
+  const unsigned ring = (unsigned)__cvta_generic_to_shared(sm) + warp * NS * TL::BYTES;
 
-  auto issue = [&](int tile, int slot) {
-    if (tile < te) {
-      const int t0 = tile * DTT, n = min(DTT, p - t0);
-      const unsigned st = sbase + slot * TL::BYTES;
-      for (int v = tid; v < 2 * DTT * PR; v += NT) {
-        const int kv = v >= DTT * PR, rem = v - kv * DTT * PR, t = rem / PR, c = rem - t * PR;
-        if (t < n) {
-          const uint16_t *src = (kv ? Vb : Kb) + (size_t)(t0 + t) * HD + c * 8;
-          cp16s(st + (kv ? DTT * TL::KROW + t * TL::VROW : t * TL::KROW) + c * 16, src);
-        }
+  // the warp's i-th tile into ring slot i % NS: 32 K rows then 32 V rows,
+  // rows past p zero-filled (their scores are masked; zero V keeps P V finite)
+  auto issue = [&](int i) {
+    if (i < nmine) {
+      const int t0 = (tb + warp + DNW * i) * DTT, n = min(DTT, p - t0);
+      const unsigned st = ring + (i % NS) * TL::BYTES;
+#pragma unroll 4
+      for (int v = lane; v < 2 * DTT * PR; v += 32) {
+        const int kv = v >= DTT * PR, rem = v - kv * DTT * PR, t = rem / PR, c = rem % PR;
+        const bool ok = t < n;
+        const uint16_t *src = (kv ? Vb : Kb) + (size_t)(t0 + (ok ? t : 0)) * HD + c * 8;
+        cp16z(st + (kv * DTT + t) * TL::ROW + c * 16, src, ok);
       }
     }
     cp_commit();
   };
 #pragma unroll
-  for (int i = 0; i < DNST - 1; ++i) issue(tb + i, i);
+  for (int i = 0; i < PF; ++i) issue(i);
 
   pdl_wait();
   pdl_trigger();
 
-  // K/V of position p itself (written by the QKV kernel this kernel follows),
-  // folded in by the last split after its tiles: loaded now, with q, so the
-  // round trip overlaps the tile loop
+  // K/V of position p (written by the QKV kernel this kernel follows), for
+  // the last split: loaded now so the round trip overlaps the tile loop
   float kp[PER], vp[PER];
-  if (sp == cs - 1) {
-    const uint16_t *kc = Kb + (size_t)p * HD + lane * PER, *vc = Vb + (size_t)p * HD + lane * PER;
+  if (last) {
+    const uint16_t *kc = Kb + (size_t)p * HD, *vc = Vb + (size_t)p * HD;
 #pragma unroll
     for (int r = 0; r < PER; ++r) {
-      kp[r] = act_to_f(kc[r], ACT);
-      vp[r] = act_to_f(vc[r], ACT);
+      kp[r] = act_to_f(kc[lane + 32 * r], ACT);
+      vp[r] = act_to_f(vc[lane + 32 * r], ACT);
     }
   }
 
-  // q of head h as 16-bit pairs (q is act-rounded after RoPE: exact)
-  const int h = g * GRP + warp;
-  const float *qp = a.q + ((size_t)b * a.H + h) * HD;
-  uint32_t qr[HD / 2];
+  // q of the kv head's GRP query heads as the A fragments of S = q K^T
+  // (row gq = head; rows 8..15 and heads >= GRP are zero; q is act-rounded
+  // after RoPE, so the 16-bit pairs are exact)
+  const float *qb = a.q + ((size_t)b * a.H + (size_t)g * GRP) * HD;
+  uint32_t qa[KS][4];
 #pragma unroll
-  for (int i = 0; i < HD / 4; ++i) {
-    const float4 v = *reinterpret_cast<const float4 *>(qp + 4 * i);
-    qr[2 * i] = pack_act2(v.x, v.y, ACT);
-    qr[2 * i + 1] = pack_act2(v.z, v.w, ACT);
+  for (int ks = 0; ks < KS; ++ks) {
+    qa[ks][0] = qa[ks][1] = qa[ks][2] = qa[ks][3] = 0u;
+    if (gq < GRP) {
+      const float2 lo = *reinterpret_cast<const float2 *>(qb + gq * HD + 16 * ks + 2 * tq);
+      const float2 hi = *reinterpret_cast<const float2 *>(qb + gq * HD + 16 * ks + 8 + 2 * tq);
+      qa[ks][0] = pack_act2(lo.x, lo.y, ACT);
+      qa[ks][2] = pack_act2(hi.x, hi.y, ACT);
+    }
   }
-  const float scale = 1.0f / sqrtf((float)HD);
-  float mrun = -INFINITY, lrun = 0.f, o[PER];
-#pragma unroll
-  for (int r = 0; r < PER; ++r) o[r] = 0.f;
+  const float sl2 = 1.4426950408889634f / sqrtf((float)HD);
 
-  if (te - tb <= DNST - 1) {
-    // Every tile of this split is in flight since before the wait: scores
-    // of all its positions first (lane j takes position j of each tile), one
-    // max and one sum, then the V pass with the final numerators.
-    cp_wait<0>();
-    __syncthreads();
-    const int nt = te - tb;
-    float sc[DNST - 1];
+  // softmax state of head gq (the same in the 4 lanes of a quad) and O^T
+  // fragments: o[mt] = rows (dims) 16 mt + gq (+8) x columns (heads) 2 tq, 2 tq + 1
+  float mrun = -INFINITY, lrun = 0.f;
+  float o[KS][4];
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+  for (int i = 0; i < nmine; ++i) {
+    if (NS > 1) {
+      cp_wait<(NS > 1 ? NS - 2 : 0)>();
+      __syncwarp();  // every lane's copies of tile i landed; slot (i - 1) % NS is free
+      issue(i + NS - 1);
+    } else {
+      cp_wait<0>();
+      __syncwarp();
+    }
+    const unsigned kt = ring + (i % NS) * TL::BYTES, vt = kt + DTT * TL::ROW;
+    const int n = min(DTT, p - (tb + warp + DNW * i) * DTT);
+
+    // S[head][t] for the tile's 32 positions: 4 n-tiles of 8
+    float s[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int kp2 = 0; kp2 < KS / 2; ++kp2) {
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        uint32_t kb[4];  // dims 32 kp2 + 8j of positions 8 nt + 0..7, j = 0..3
+        ldsm_x4(kb, kt + (8 * nt + (lane & 7)) * TL::ROW + (32 * kp2 + 8 * (lane >> 3)) * 2);
+        mma16816<ACT>(s[nt], qa[2 * kp2], kb);
+        mma16816<ACT>(s[nt], qa[2 * kp2 + 1], kb + 2);
+      }
+    }
+    // online softmax of head gq over positions 8 nt + 2 tq + {0, 1}
     float mx = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < DNST - 1; ++i) {
-      sc[i] = -INFINITY;
-      const int n = i < nt ? min(DTT, p - (tb + i) * DTT) : 0;
-      if (lane < n) sc[i] = k_dot_q<HD, ACT>(sm + i * TL::BYTES + lane * TL::KROW, qr) * scale;
-      mx = fmaxf(mx, sc[i]);
-    }
-    mx = warp_max(mx);
-    float *pw = pbuf + warp * DNST * DTT;
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float v = 8 * nt + 2 * tq + j < n ? s[nt][j] * sl2 : -INFINITY;
+        s[nt][j] = v;
+        mx = fmaxf(mx, v);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mnew = fmaxf(mrun, mx);  // finite: the tile has a position < p
+    const float corr = exp2f(mrun - mnew);
+    uint32_t ph[2][2], pl[2][2];  // P^T as B fragments: k-step kk = positions 16 kk + ...
     float ls = 0.f;
 #pragma unroll
-    for (int i = 0; i < DNST - 1; ++i) {
-      const float pe = sc[i] == -INFINITY ? 0.f : expf(sc[i] - mx);
-      pw[i * DTT + lane] = pe;
-      ls += pe;
+    for (int nt = 0; nt < 4; ++nt) {
+      const float p0 = exp2f(s[nt][0] - mnew), p1 = exp2f(s[nt][1] - mnew);
+      ls += p0 + p1;
+      const uint32_t hw = pack_act2(p0, p1, ACT);
+      ph[nt >> 1][nt & 1] = hw;
+      pl[nt >> 1][nt & 1] = pack_act2(p0 - act_to_f((uint16_t)(hw & 0xffffu), ACT),
+                                      p1 - act_to_f((uint16_t)(hw >> 16), ACT), ACT);
     }
-    ls = warp_sum(ls);
-    __syncwarp();
-    for (int i = 0; i < nt; ++i)
-      v_accumulate<HD, ACT>(sm + i * TL::BYTES + DTT * TL::KROW, pw + i * DTT, min(DTT, p - (tb + i) * DTT), lane, o);
-    if (nt > 0) {
-      mrun = mx;
-      lrun = ls;
-    }
-  } else {
-    for (int tile = tb, it = 0; tile < te; ++tile, ++it) {
-      cp_wait<DNST - 2>();
-      __syncthreads();  // the tile is in; every warp is done with the slot refilled next
-      issue(tile + DNST - 1, (it + DNST - 1) % DNST);
-      const unsigned char *tk = sm + (it % DNST) * TL::BYTES;
-      const unsigned char *tv = tk + DTT * TL::KROW;
-      const int n = min(DTT, p - tile * DTT);
-      float sc = -INFINITY;
-      if (lane < n) sc = k_dot_q<HD, ACT>(tk + lane * TL::KROW, qr) * scale;
-      const float mnew = fmaxf(mrun, warp_max(sc));
-      const float pe = lane < n ? expf(sc - mnew) : 0.f;
-      const float corr = mrun == -INFINITY ? 0.f : expf(mrun - mnew);
-      lrun = lrun * corr + warp_sum(pe);
-#pragma unroll
-      for (int r = 0; r < PER; ++r) o[r] *= corr;
-      float *pw = pbuf + warp * DNST * DTT;
-      pw[lane] = pe;
-      __syncwarp();
-      v_accumulate<HD, ACT>(tv, pw, n, lane, o);
-      __syncwarp();  // pw is rewritten by the next tile
-      mrun = mnew;
-    }
-  }
-
-  // position p itself (its K/V were written by the QKV kernel this kernel
-  // follows): folded in by the last split
-  if (sp == cs - 1) {
-    float d = 0.f;
-#pragma unroll
-    for (int r = 0; r < PER; ++r) d = fmaf(qp[lane * PER + r], kp[r], d);
-    const float sc = warp_sum(d) * scale;
-    const float mnew = fmaxf(mrun, sc);
-    const float corr = mrun == -INFINITY ? 0.f : expf(mrun - mnew), pe = expf(sc - mnew);
-    lrun = lrun * corr + pe;
-#pragma unroll
-    for (int r = 0; r < PER; ++r) o[r] = fmaf(pe, vp[r], o[r] * corr);
+    ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+    lrun = fmaf(lrun, corr, ls);
     mrun = mnew;
+    // rescale O^T: its columns are heads 2 tq and 2 tq + 1, whose factors sit
+    // in quads 2 tq and 2 tq + 1
+    const float ca = __shfl_sync(0xffffffffu, corr, 8 * tq), cb = __shfl_sync(0xffffffffu, corr, 8 * tq + 4);
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      o[mt][0] *= ca;
+      o[mt][1] *= cb;
+      o[mt][2] *= ca;
+      o[mt][3] *= cb;
+    }
+    // O^T += V^T P^T
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        uint32_t va[4];  // V^T rows 16 mt + 0..15 x positions 16 kk + 0..15
+        ldsm_x4_t(va, vt + (16 * kk + 8 * (lane >> 4) + (lane & 7)) * TL::ROW + (16 * mt + 8 * ((lane >> 3) & 1)) * 2);
+        mma16816<ACT>(o[mt], va, ph[kk]);
+        mma16816<ACT>(o[mt], va, pl[kk]);
+      }
+    if (NS == 1) {
+      __syncwarp();  // every lane is done with the slot before it is refilled
+      issue(i + 1);
+    }
+  }
+  cp_wait<0>();
+  __syncthreads();  // every warp is done with its ring: the merge reuses it
+
+  float *part = reinterpret_cast<float *>(sm);
+  float *wpo = part + GRP * HD;
+  float *pm = wpo + DNW * GRP * HD;
+  float *wml = pm + 2 * GRP;
+  float *sps = wml + DNW * GRP * 2;
+  float *spv = sps + GRP;
+  float *gml = spv + HD;
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    const int d = 16 * mt + gq, h0 = 2 * tq, h1 = 2 * tq + 1;
+    if (h0 < GRP) {
+      wpo[(warp * GRP + h0) * HD + d] = o[mt][0];
+      wpo[(warp * GRP + h0) * HD + d + 8] = o[mt][2];
+    }
+    if (h1 < GRP) {
+      wpo[(warp * GRP + h1) * HD + d] = o[mt][1];
+      wpo[(warp * GRP + h1) * HD + d + 8] = o[mt][3];
+    }
+  }
+  if (tq == 0 && gq < GRP) {
+    wml[(warp * GRP + gq) * 2] = mrun;
+    wml[(warp * GRP + gq) * 2 + 1] = lrun;
+  }
+  if (last) {
+    for (int hh = warp; hh < GRP; hh += DNW) {
+      float d = 0.f;
+#pragma unroll
+      for (int r = 0; r < PER; ++r) d = fmaf(qb[hh * HD + lane + 32 * r], kp[r], d);
+      d = warp_sum(d);
+      if (lane == 0) sps[hh] = d * sl2;
+    }
+    if (warp == 0) {
+#pragma unroll
+      for (int r = 0; r < PER; ++r) spv[lane + 32 * r] = vp[r];
+    }
+  }
+  __syncthreads();
+
+  // the block's state per head: its warps, plus position p in the last split
+  for (int it = tid; it < GRP * HD; it += DNW * 32) {
+    const int h = it / HD, d = it - h * HD;
+    float M = last ? sps[h] : -INFINITY;
+#pragma unroll
+    for (int w = 0; w < DNW; ++w) M = fmaxf(M, wml[(w * GRP + h) * 2]);
+    float acc = 0.f, Ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < DNW; ++w) {
+      const float mw = wml[(w * GRP + h) * 2];
+      const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      acc = fmaf(wt, wpo[(w * GRP + h) * HD + d], acc);
+      Ls = fmaf(wt, wml[(w * GRP + h) * 2 + 1], Ls);
+    }
+    if (last) {
+      const float wt = exp2f(sps[h] - M);
+      acc = fmaf(wt, spv[d], acc);
+      Ls += wt;
+    }
+    part[h * HD + d] = acc;
+    if (d == 0) {
+      pm[2 * h] = M;
+      pm[2 * h + 1] = Ls;
+    }
   }
 
-  // merge across the cluster: split sp combines dims [sp * HD / cs, ...) of
-  // every head.  Warp hh takes head hh; lane l < HD / 4 reads split
-  // r = l % cs (its max, sum and 4 dims of o, from that block's shared
-  // memory), so all the remote loads are in flight at once, and the cs lanes
-  // of a 4-dim block combine by shuffles.
-  float *pm = part + GRP * HD;
-#pragma unroll
-  for (int r = 0; r < PER; ++r) part[warp * HD + lane * PER + r] = o[r];
-  if (lane == 0) {
-    pm[warp * 2] = mrun;
-    pm[warp * 2 + 1] = lrun;
+  float *out = a.o + ((size_t)b * a.H + (size_t)g * GRP) * HD;
+  if (GM) {
+    __syncthreads();
+    if (cs == 1) {  // the only split: the block's state is the result
+      for (int it = tid; it < GRP * HD; it += DNW * 32)
+        out[it] = round_act(part[it] / pm[2 * (it / HD) + 1], ACT);
+      return;
+    }
+    // publish (O, max, sum) of this split; the last block of (row, kv head)
+    // to arrive merges every split's state
+    float *gp = a.part + ((size_t)(b * a.Hkv + g) * cs) * GRP * (HD + 2);
+    for (int it = tid; it < GRP * HD; it += DNW * 32) {
+      const int h = it / HD, d = it - h * HD;
+      gp[((size_t)sp * GRP + h) * (HD + 2) + d] = part[it];
+    }
+    if (tid < 2 * GRP) gp[((size_t)sp * GRP + tid / 2) * (HD + 2) + HD + (tid & 1)] = pm[tid];
+    __threadfence();
+    __syncthreads();
+    int *flag = reinterpret_cast<int *>(gml + cs * GRP * 2);
+    if (tid == 0) {
+      unsigned *ctr = a.counter + b * a.Hkv + g;
+      const unsigned t = atomicAdd(ctr, 1u);
+      const int am_last = t == (unsigned)(cs - 1);
+      if (am_last) *ctr = 0u;  // left at zero for the next launch
+      *flag = am_last;
+    }
+    __syncthreads();
+    if (!*flag) return;
+    __threadfence();
+    for (int it = tid; it < cs * GRP * 2; it += DNW * 32)
+      gml[it] = __ldcg(gp + (size_t)(it >> 1) * (HD + 2) + HD + (it & 1));
+    __syncthreads();
+    for (int it = tid; it < GRP * HD; it += DNW * 32) {
+      const int h = it / HD, d = it - h * HD;
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < cs; ++s2) M = fmaxf(M, gml[(s2 * GRP + h) * 2]);
+      float acc = 0.f, Ls = 0.f;
+      for (int s2 = 0; s2 < cs; ++s2) {
+        const float ms = gml[(s2 * GRP + h) * 2];
+        const float wt = ms == -INFINITY ? 0.f : exp2f(ms - M);
+        acc = fmaf(wt, __ldcg(gp + ((size_t)s2 * GRP + h) * (HD + 2) + d), acc);
+        Ls = fmaf(wt, gml[(s2 * GRP + h) * 2 + 1], Ls);
+      }
+      out[it] = round_act(acc / Ls, ACT);
+    }
+    return;
+  } else {
+    // merge across the cluster: split sp combines dims [sp * HD / cs, ...) of
+    // every head.  Lane l < HD / 4 reads split r = l % cs (its max, sum and 4
+    // dims of O, from that block's shared memory), so all the remote loads
+    // are in flight at once, and the cs lanes of a 4-dim block combine by
+    // shuffles.
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();
+    for (int hh = warp; hh < GRP; hh += DNW) {
+      const int dpc = HD / cs, r = lane % cs, d0 = sp * dpc + (lane / cs) * 4;
+      const bool live = lane < HD / 4;
+      float m = -INFINITY, l = 0.f;
+      float4 ov = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (live) {
+        const float *rp = cl.map_shared_rank(part, r);
+        const float *rm = cl.map_shared_rank(pm, r);
+        m = rm[hh * 2];
+        l = rm[hh * 2 + 1];
+        ov = *reinterpret_cast<const float4 *>(rp + hh * HD + d0);
+      }
+      float M = m;
+      for (int x = 1; x < cs; x <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+      float Ls = w * l, o0 = w * ov.x, o1 = w * ov.y, o2 = w * ov.z, o3 = w * ov.w;
+      for (int x = 1; x < cs; x <<= 1) {
+        Ls += __shfl_xor_sync(0xffffffffu, Ls, x);
+        o0 += __shfl_xor_sync(0xffffffffu, o0, x);
+        o1 += __shfl_xor_sync(0xffffffffu, o1, x);
+        o2 += __shfl_xor_sync(0xffffffffu, o2, x);
+        o3 += __shfl_xor_sync(0xffffffffu, o3, x);
+      }
+      if (live && r == 0) {
+        const float inv = 1.0f / Ls;
+        float *dst = out + hh * HD + d0;
+        dst[0] = round_act(o0 * inv, ACT);
+        dst[1] = round_act(o1 * inv, ACT);
+        dst[2] = round_act(o2 * inv, ACT);
+        dst[3] = round_act(o3 * inv, ACT);
+      }
+    }
+    cl.sync();  // every split's partials stay readable until all merges are done
   }
-  cl.sync();
-  {
-    const int dpc = HD / cs, r = lane % cs, d0 = sp * dpc + (lane / cs) * 4;
-    const bool live = lane < HD / 4;
-    float m = -INFINITY, l = 0.f;
-    float4 ov = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live) {
-      const float *rp = cl.map_shared_rank(part, r);
-      m = rp[GRP * HD + warp * 2];
-      l = rp[GRP * HD + warp * 2 + 1];
-      ov = *reinterpret_cast<const float4 *>(rp + warp * HD + d0);
-    }
-    float M = m;
-    for (int x = 1; x < cs; x <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
-    const float w = m == -INFINITY ? 0.f : expf(m - M);
-    float Ls = w * l, o0 = w * ov.x, o1 = w * ov.y, o2 = w * ov.z, o3 = w * ov.w;
-    for (int x = 1; x < cs; x <<= 1) {
-      Ls += __shfl_xor_sync(0xffffffffu, Ls, x);
-      o0 += __shfl_xor_sync(0xffffffffu, o0, x);
-      o1 += __shfl_xor_sync(0xffffffffu, o1, x);
-      o2 += __shfl_xor_sync(0xffffffffu, o2, x);
-      o3 += __shfl_xor_sync(0xffffffffu, o3, x);
-    }
-    if (live && r == 0) {
-      const float inv = 1.0f / Ls;
-      float *dst = a.o + ((size_t)b * a.H + g * GRP + warp) * HD + d0;
-      dst[0] = round_act(o0 * inv, ACT);
-      dst[1] = round_act(o1 * inv, ACT);
-      dst[2] = round_act(o2 * inv, ACT);
-      dst[3] = round_act(o3 * inv, ACT);
-    }
-  }
-  cl.sync();  // every split's partials stay readable until all merges are done
 }
 
-template <int HD, int GRP, int ACT>
+template <int HD, int GRP, int ACT, int NS, bool GM>
 static cudaError_t launch_dec(const AttnArgs &a, int B, int cs, cudaStream_t s, int pdl) {
-  auto fn = k_attn_dec<HD, GRP, ACT>;
-  const size_t smem = dec_smem<HD>(GRP);
+  auto fn = k_attn_dec<HD, GRP, ACT, NS, GM>;
+  const size_t smem = dec_smem<HD, NS>(GRP);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess && cs > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess && !GM && cs > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, a.Hkv, B);
-  cfg.blockDim = dim3(GRP * 32);
+  cfg.blockDim = dim3(DNW * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  int na = 0;
+  if (!GM) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cs;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
+  cfg.numAttrs = na;
   e = cudaLaunchKernelEx(&cfg, fn, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Launch plan of the decode attention for B rows whose longest context is
+// pmax positions: clusters of splits while each warp of a split has at most
+// one tile (returns 0, *splits = cluster size), else about one block per SM
+// merged through global memory (returns 1, *splits = blocks per (row, kv
+// head), at most max_splits).
+int attn_dec_plan(int B, int Hkv, int n_sm, int max_cluster, int max_splits, int pmax, int *splits) {
+  int cs = 1;
+  while (2 * cs <= max_cluster && 2 * cs * Hkv * B <= 2 * n_sm) cs *= 2;
+  const int ntile = (pmax + DTT - 1) / DTT;
+  if ((ntile + cs - 1) / cs <= DNW) {
+    *splits = cs;
+    return 0;
+  }
+  int S = n_sm / (Hkv * B);
+  if (S > max_splits) S = max_splits;
+  if (S > kAttnMaxSplits) S = kAttnMaxSplits;
+  if (S < 1) S = 1;
+  *splits = S;
+  return 1;
 }
 
 // Largest cluster size (power of two, <= 16) the decode attention can be
@@ -437,7 +607,7 @@ int attn_dec_max_cluster(int hd, int grp, int act) {
   for (int cs = 16; cs >= 1; cs >>= 1) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs, 1, 1);
-    cfg.blockDim = dim3(grp * 32);
+    cfg.blockDim = dim3(DNW * 32);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
@@ -449,8 +619,8 @@ int attn_dec_max_cluster(int hd, int grp, int act) {
     cudaError_t e = cudaErrorInvalidValue;
 #define RV_DQ(HD_, G_, A_)                                                                                   \
   if (hd == HD_ && grp == G_ && act == A_) {                                                                 \
-    auto fn = k_attn_dec<HD_, G_, A_>;                                                                       \
-    cfg.dynamicSmemBytes = dec_smem<HD_>(G_);                                                                \
+    auto fn = k_attn_dec<HD_, G_, A_, 1, false>;                                                             \
+    cfg.dynamicSmemBytes = dec_smem<HD_, 1>(G_);                                                             \
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);    \
     if (e == cudaSuccess && cs > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1); \
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);                                  \
@@ -485,34 +655,6 @@ struct PreTile {
   static constexpr int KV = PK * ROW;
   static constexpr int BYTES = 2 * KV;
 };
-
-__device__ __forceinline__ void cp16z(unsigned dst, const void *src, bool valid) {
-  const int n = valid ? 16 : 0;  // 0: zero-fill, nothing read
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t *r, unsigned addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t *r, unsigned addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-template <int ACT>
-__device__ __forceinline__ void mma16816(float *d, const uint32_t *a, const uint32_t *b) {
-  if (ACT == 1)
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-  else
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
 
 template <int HD, int GRP, int ACT>
 __global__ void __launch_bounds__(GRP * 32) k_attn_prefill(AttnRowsArgs a, int T) {
@@ -691,14 +833,26 @@ static cudaError_t launch_any(const AttnArgs &a, int T_per_row, const int32_t *b
   return cudaErrorInvalidValue;
 }
 
-// Decode: one row per batch entry, the token at position len[b]; a.splits is
-// the cluster size (a power of two <= 16 that attn_dec_max_cluster allows).
+// Decode: one row per batch entry, the token at position len[b].
+// a.global_merge = 0: a.splits is the cluster size (a power of two <= 16 that
+// attn_dec_max_cluster allows); 1: a.splits blocks per (row, kv head),
+// 1..kAttnMaxSplits, merged through a.part / a.counter.
 cudaError_t launch_attn_decode(const AttnArgs &a, int B, cudaStream_t s, int pdl) {
   const int grp = a.H / a.Hkv, cs = a.splits;
-  if (cs < 1 || cs > 16 || (cs & (cs - 1))) return cudaErrorInvalidValue;
-#define RV_DL(HD_, G_)                                                                  \
-  if (a.hd == HD_ && grp == G_)                                                         \
-    return a.act == 1 ? launch_dec<HD_, G_, 1>(a, B, cs, s, pdl) : launch_dec<HD_, G_, 0>(a, B, cs, s, pdl);
+  if (a.global_merge) {
+    if (cs < 1 || cs > kAttnMaxSplits) return cudaErrorInvalidValue;
+  } else if (cs < 1 || cs > 16 || (cs & (cs - 1))) {
+    return cudaErrorInvalidValue;
+  }
+#define RV_DL(HD_, G_)                                                                                   \
+  if (a.hd == HD_ && grp == G_) {                                                                        \
+    constexpr int NSL = DecTile<HD_>::NS_LONG;                                                           \
+    if (a.global_merge)                                                                                  \
+      return a.act == 1 ? launch_dec<HD_, G_, 1, NSL, true>(a, B, cs, s, pdl)                            \
+                        : launch_dec<HD_, G_, 0, NSL, true>(a, B, cs, s, pdl);                           \
+    return a.act == 1 ? launch_dec<HD_, G_, 1, 1, false>(a, B, cs, s, pdl)                               \
+                      : launch_dec<HD_, G_, 0, 1, false>(a, B, cs, s, pdl);                              \
+  }
   RV_DL(64, 1) RV_DL(64, 2) RV_DL(64, 4) RV_DL(64, 8)
   RV_DL(128, 1) RV_DL(128, 2) RV_DL(128, 4) RV_DL(128, 8)
 #undef RV_DL

@@ -1,5 +1,5 @@
-// Batch-1 GEMV core shared by the per-kernel decode chain (decode_b1.cu) and
-// the persistent decode-step kernel (mega.cu).  Internal header.
+// Batch-1 GEMV core of the per-kernel decode chain (decode_b1.cu).
+// Internal header.
 //
 // A warp owns 4 output rows (a "quad") and, when a matrix has too few quads to
 // fill the GPU, one of S splits of its K chunks (S warps of a block per quad).

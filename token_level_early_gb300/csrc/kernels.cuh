@@ -111,12 +111,17 @@ struct AttnArgs {
   float *o;            // [B][H*hd] output (act16-rounded)
   const int32_t *len;  // [B]: the token being decoded sits at position len[b]
   int splits;
-  float *part;         // [B][H][splits][hd + 2]
-  unsigned *counter;   // [B][Hkv]
+  float *part;         // [B][Hkv][splits][H / Hkv][hd + 2] (global merge)
+  unsigned *counter;   // [B][Hkv], zero between launches (global merge)
+  int global_merge;    // 0: the splits form a cluster; 1: they merge through part / counter
 };
+constexpr int kAttnMaxSplits = 128;
 cudaError_t launch_attn_decode(const AttnArgs &a, int B, cudaStream_t s, int pdl = 0);
 // Largest cluster size (power of two <= 16) launch_attn_decode can use; 0 if none.
 int attn_dec_max_cluster(int hd, int grp, int act);
+// Launch plan for B rows whose longest context is pmax positions: returns
+// AttnArgs::global_merge and sets *splits.
+int attn_dec_plan(int B, int Hkv, int n_sm, int max_cluster, int max_splits, int pmax, int *splits);
 
 // Causal attention for token rows of the general path: row m of the list
 // attends to positions 0..pos(m) of its sequence.
@@ -153,6 +158,20 @@ cudaError_t launch_gemm_tc(const Mat &m, int act, const float *X, float *Y, cons
 cudaError_t launch_gemm_tc_river(const Mat &m, int act, const float *X, float *Y, const int32_t *list,
                                  const int32_t *count, int max_rows, uint16_t *xb, uint16_t *whi, uint16_t *wlo,
                                  int32_t *err, cudaStream_t s);
+// Batched decode rows on the tensor pipe (mma.sync): Y[list[i]] = W X[list[i]]
+// for the river copy ((q - z) s, groups of 32, 64, 128 or 256; fewer than 256
+// rows) or the 16-bit matrix (at most 64 rows).
+bool rows_i4_supported(const Mat &m);
+bool rows_b16_supported(const Mat &m);
+cudaError_t launch_rows_i4(const Mat &m, int act, const float *X, float *Y, const int32_t *list,
+                           const int32_t *count, int max_rows, int n_sm, cudaStream_t s);
+// amax (optional, [rows]): each row's greedy pick as a key (largest value,
+// lowest column on ties), for launch_pick_finish; zero before the launch.
+cudaError_t launch_rows_b16(const Mat &m, int act, const float *X, float *Y, const int32_t *list,
+                            const int32_t *count, int max_rows, int n_sm, cudaStream_t s,
+                            unsigned long long *amax = nullptr);
+cudaError_t launch_pick_finish(unsigned long long *amax, int B, StepState st, int bump_len, int set_len,
+                               cudaStream_t s);
 cudaError_t launch_gemm_rows(const Mat &m, int river, int act, const float *X, float *Y, const int32_t *list,
                              const int32_t *count, int max_rows, cudaStream_t s);
 struct RopeRowsArgs {
