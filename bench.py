@@ -10,7 +10,7 @@ prompt, tau = 0.90; the Llama-3.2-1B-shaped workload is reported beside it.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload llama8b|llama1b|layer8b] [--modes tau,forced,full,river]
                   [--engine chain|persistent] [--no-cpu-baseline] [--no-secondary]
-                  [--no-fidelity] [--no-extra] [--only batch64|long64k]
+                  [--no-fidelity] [--no-extra] [--only batch64|long64k] [--prompt-len N]
 
 value : decode tokens/s, device-timed with CUDA events on the model's stream;
         tokens chained on the device (step i+1 consumes step i's id).
@@ -281,7 +281,7 @@ def run_workload(wl_name, steps, warmup, dev_index, want_cpu, rank0, log, modes=
     # backbone offloading (the pages' parameter-memory comparison): keep the
     # first backbone layers on the device, cap the exits there, decode on
     offload = None
-    if want_offload:
+    if want_offload and L > 3:
         keep = 3
         full_bytes = m.param_bytes(0) + m.param_bytes(1)
         m.offload_backbone(keep)
@@ -597,6 +597,8 @@ def main():
     ap.add_argument("--no-fidelity", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the batch-64 and 64K-context workloads")
+    ap.add_argument("--prompt-len", type=int, default=0,
+                    help="override the workload's prompt length (profiling cases, e.g. long-context attention)")
     ap.add_argument("--only", choices=["batch64", "long64k"],
                     help="time only this workload (its own JSON line; for profiling commands)")
     args = ap.parse_args()
@@ -608,6 +610,10 @@ def main():
         if rank0:
             print(msg, file=sys.stderr, flush=True)
 
+    if args.prompt_len > 0:
+        import dataclasses
+        synth.WORKLOADS[args.workload] = dataclasses.replace(synth.WORKLOADS[args.workload],
+                                                             prompt_len=args.prompt_len)
     wl = synth.WORKLOADS[args.workload]
     tau = wl.taus[0] if wl.taus else 0.90
     cfg = {"workload": f"{wl.shape.name} decode, batch 1, {wl.prompt_len}-token random prompt, tau {tau}, "

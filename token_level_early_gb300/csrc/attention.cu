@@ -582,18 +582,20 @@ static cudaError_t launch_dec(const AttnArgs &a, int B, int cs, cudaStream_t s, 
 
 // Launch plan of the decode attention for B rows whose longest context is
 // pmax positions: clusters of splits while each warp of a split has at most
-// one tile (returns 0, *splits = cluster size), else about one block per SM
-// merged through global memory (returns 1, *splits = blocks per (row, kv
-// head), at most max_splits).
+// one tile, or while the rows alone fill the GPU (B x Hkv >= n_sm / 2: small
+// blocks, many resident per SM) (returns 0, *splits = cluster size); else
+// about one block per SM per (row, kv head) split, merged through global
+// memory (returns 1, *splits = blocks per (row, kv head), at most
+// max_splits).
 int attn_dec_plan(int B, int Hkv, int n_sm, int max_cluster, int max_splits, int pmax, int *splits) {
   int cs = 1;
   while (2 * cs <= max_cluster && 2 * cs * Hkv * B <= 2 * n_sm) cs *= 2;
   const int ntile = (pmax + DTT - 1) / DTT;
-  if ((ntile + cs - 1) / cs <= DNW) {
+  int S = n_sm / (Hkv * B);
+  if ((ntile + cs - 1) / cs <= DNW || S < 2) {
     *splits = cs;
     return 0;
   }
-  int S = n_sm / (Hkv * B);
   if (S > max_splits) S = max_splits;
   if (S > kAttnMaxSplits) S = kAttnMaxSplits;
   if (S < 1) S = 1;

@@ -112,10 +112,16 @@ __global__ void k_pack_rows(const float *X, int K, int act, const int32_t *list,
 template <int ACT>
 __global__ void __launch_bounds__(128, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, float *Y, int N, int K,
-              const int32_t *list, const int32_t *count, int32_t *err, int accumulate) {
+              const int32_t *list, const int32_t *count, int32_t *err, int accumulate, int mtiles, int gm) {
   const int cnt = *count;
-  // row tiles vary fastest: the CTAs resident at a time share weight tiles in L2
-  const int m0 = blockIdx.x * TBM, n0 = blockIdx.y * TBN;
+  // Grouped raster over a 1-D grid: groups of gm row tiles, and within a
+  // group the row tiles vary fastest.  The CTAs resident at a time then share
+  // weight tiles, and a group's gm row tiles of X stay in L2 while the group
+  // walks every weight tile: X is read from DRAM once and W once per group.
+  const int ntiles = (N + TBN - 1) / TBN;
+  const int per_group = gm * ntiles, grp = blockIdx.x / per_group, in = blockIdx.x - grp * per_group;
+  const int first = grp * gm, rows_here = min(gm, mtiles - first);
+  const int m0 = (first + in % rows_here) * TBM, n0 = (in / rows_here) * TBN;
   if (m0 >= cnt) return;  // no listed row in this tile (before any allocation)
   extern __shared__ uint8_t smraw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -287,15 +293,23 @@ cudaError_t gemm_tc_run(const void *W, int N, int K, int act, float *Y, const in
                         int max_rows, const uint16_t *xb, int32_t *err, int accumulate, cudaStream_t s) {
   CUtensorMap ta, tb;
   if (!make_map(&ta, xb, max_rows, K, act) || !make_map(&tb, W, N, K, act)) return cudaErrorInvalidValue;
-  dim3 grid((max_rows + TBM - 1) / TBM, (N + TBN - 1) / TBN);
-  if (grid.y > 65535) return cudaErrorInvalidValue;
+  const long mtiles = (max_rows + TBM - 1) / TBM, ntiles = (N + TBN - 1) / TBN;
+  if (mtiles * ntiles > 0x7FFFFFFFL) return cudaErrorInvalidValue;
+  // row tiles per group: their X tiles (TBM x K 16-bit each) within ~64 MB of L2
+  const long tile_bytes = (long)TBM * K * 2;
+  long gm = (64L << 20) / (tile_bytes > 0 ? tile_bytes : 1);
+  if (gm < 1) gm = 1;
+  if (gm > mtiles) gm = mtiles;
+  const dim3 grid((unsigned)(mtiles * ntiles));
   cudaError_t e;
   if (act == 1) {
     e = cudaFuncSetAttribute(k_gemm_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TSMEM);
-    if (e == cudaSuccess) k_gemm_tc<1><<<grid, 128, TSMEM, s>>>(ta, tb, Y, N, K, list, count, err, accumulate);
+    if (e == cudaSuccess)
+      k_gemm_tc<1><<<grid, 128, TSMEM, s>>>(ta, tb, Y, N, K, list, count, err, accumulate, (int)mtiles, (int)gm);
   } else {
     e = cudaFuncSetAttribute(k_gemm_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TSMEM);
-    if (e == cudaSuccess) k_gemm_tc<0><<<grid, 128, TSMEM, s>>>(ta, tb, Y, N, K, list, count, err, accumulate);
+    if (e == cudaSuccess)
+      k_gemm_tc<0><<<grid, 128, TSMEM, s>>>(ta, tb, Y, N, K, list, count, err, accumulate, (int)mtiles, (int)gm);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
