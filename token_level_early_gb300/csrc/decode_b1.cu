@@ -26,10 +26,10 @@
 
 namespace rv {
 
-constexpr int NW = 8;  // warps per block
+constexpr int NW = 16;  // warps per block: one block per SM (the SM frees at once for the next kernel)
 
 template <int ACT, int PRO, int EPI>
-__global__ void __launch_bounds__(NW * 32, 2) k_gemv_b1(GemvArgs a) {
+__global__ void __launch_bounds__(NW * 32, 1) k_gemv_b1(GemvArgs a) {
   extern __shared__ __align__(16) float smem[];
   const Geo g = geo_of(a.m);
   const int tid = threadIdx.x, warp = tid >> 5;
