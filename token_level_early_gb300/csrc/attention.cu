@@ -547,10 +547,29 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
   }
 }
 
+// Short-context launches whose blocks all fit two per SM reserve this much
+// shared memory per block, so that at most two share an SM: the splits
+// spread over twice as many SMs as at three per SM (8B decode step: tau
+// 503 -> 515 tokens/s; one block per SM is slower again: clusters of 16
+// then need 16 free SMs in one GPC).
+constexpr size_t kDecSpreadSmem = 80 * 1024;
+
+static int device_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n < 1) n = 1;
+  }
+  return n;
+}
+
 template <int HD, int GRP, int ACT, int NS, bool GM>
 static cudaError_t launch_dec(const AttnArgs &a, int B, int cs, cudaStream_t s, int pdl) {
   auto fn = k_attn_dec<HD, GRP, ACT, NS, GM>;
-  const size_t smem = dec_smem<HD, NS>(GRP);
+  size_t smem = dec_smem<HD, NS>(GRP);
+  if (!GM && (long)cs * a.Hkv * B <= 2L * device_sms() && smem < kDecSpreadSmem) smem = kDecSpreadSmem;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess && !GM && cs > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
@@ -622,7 +641,7 @@ int attn_dec_max_cluster(int hd, int grp, int act) {
 #define RV_DQ(HD_, G_, A_)                                                                                   \
   if (hd == HD_ && grp == G_ && act == A_) {                                                                 \
     auto fn = k_attn_dec<HD_, G_, A_, 1, false>;                                                             \
-    cfg.dynamicSmemBytes = dec_smem<HD_, 1>(G_);                                                             \
+    cfg.dynamicSmemBytes = dec_smem<HD_, 1>(G_) > kDecSpreadSmem ? dec_smem<HD_, 1>(G_) : kDecSpreadSmem;   \
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);    \
     if (e == cudaSuccess && cs > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1); \
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);                                  \
