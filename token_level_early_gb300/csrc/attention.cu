@@ -173,7 +173,7 @@ __device__ __forceinline__ uint32_t pack_act2(float lo, float hi, int act) {
 }
 
 // ---- decode: split-KV attention on the tensor pipe -------------------------
-// Block (split sp, kv head g, row b) of DNW warps.  The split's tiles of 32
+// Block (split sp, kv head g, row b) of NW warps.  The split's tiles of TT
 // past positions are dealt round-robin to its warps; each warp streams its
 // own tiles through a private cp.async ring of NS slots (no block barrier in
 // the loop), the first ones issued before the programmatic-dependent-launch
@@ -193,37 +193,45 @@ __device__ __forceinline__ uint32_t pack_act2(float lo, float hi, int act) {
 //   long contexts (GM = true): no cluster, about one block per SM with a deep
 //     ring, the splits' states go through global memory and the last block of
 //     a (row, kv head) to finish merges them (an atomic ticket, no waiting).
-constexpr int DTT = 32;  // positions per tile
-constexpr int DNW = 4;   // warps per block
+// Two block shapes: short contexts (the cluster plan) 4 warps x tiles of 32
+// positions x 1 ring slot per warp (a warp holds at most one tile); long
+// contexts (the global-merge plan) 8 warps x tiles of 16 positions x a
+// multi-slot ring, the same bytes in flight per SM with twice the warps to
+// run the tile math (one warp per scheduler left the issue slots 2/3 idle).
+constexpr int DTT = 32;  // positions per tile, short plan
+constexpr int DNW = 4;   // warps per block, short plan
+constexpr int LTT = 16;  // positions per tile, long plan
+constexpr int LNW = 8;   // warps per block, long plan
 
-template <int HD>
+template <int HD, int TT>
 struct DecTile {
-  static constexpr int ROW = HD * 2 + 16;           // padded row: the 8 rows of an ldmatrix hit distinct banks
-  static constexpr int BYTES = 2 * DTT * ROW;       // K rows then V rows
-  static constexpr int NS_LONG = HD == 64 ? 6 : 3;  // ring slots per warp, long contexts
+  static constexpr int ROW = HD * 2 + 16;      // padded row: the 8 rows of an ldmatrix hit distinct banks
+  static constexpr int BYTES = 2 * TT * ROW;   // K rows then V rows
 };
+template <int HD>
+constexpr int long_slots() { return HD == 64 ? 6 : 3; }  // ring slots per warp, long plan
 
 // Merge-phase layout (floats, over the ring once it is drained):
 //   part [GRP][HD]       the block's O (read by the other splits)
-//   wpo  [DNW][GRP][HD]  the warps' O
+//   wpo  [NW][GRP][HD]   the warps' O
 //   pm   [GRP][2]        the block's (max, sum) (read by the other splits)
-//   wml  [DNW][GRP][2]   the warps' (max, sum)
+//   wml  [NW][GRP][2]    the warps' (max, sum)
 //   sps  [GRP]           score of position p;  spv [HD] its V row
 //   gml  [splits][GRP][2] the splits' (max, sum), then the last-block flag (global merge)
-template <int HD>
+template <int HD, int NW>
 __host__ __device__ constexpr int dec_merge_floats(int grp) {
-  return (1 + DNW) * grp * HD + 2 * grp + DNW * grp * 2 + grp + HD + kAttnMaxSplits * grp * 2 + 1;
+  return (1 + NW) * grp * HD + 2 * grp + NW * grp * 2 + grp + HD + kAttnMaxSplits * grp * 2 + 1;
 }
-template <int HD, int NS>
+template <int HD, int NW, int TT, int NS>
 static size_t dec_smem(int grp) {
-  const size_t merge = sizeof(float) * (size_t)dec_merge_floats<HD>(grp);
-  const size_t ring = (size_t)DNW * NS * DecTile<HD>::BYTES;
+  const size_t merge = sizeof(float) * (size_t)dec_merge_floats<HD, NW>(grp);
+  const size_t ring = (size_t)NW * NS * DecTile<HD, TT>::BYTES;
   return merge > ring ? merge : ring;
 }
 
-template <int HD, int GRP, int ACT, int NS, bool GM>
-__global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
-  using TL = DecTile<HD>;
+template <int HD, int GRP, int ACT, int NW, int TT, int NS, bool GM>
+__global__ void __launch_bounds__(NW * 32, 1) k_attn_dec(AttnArgs a) {
+  using TL = DecTile<HD, TT>;
   constexpr int KS = HD / 16, PR = HD / 8, PER = HD / 32;
   constexpr int PF = NS > 1 ? NS - 1 : 1;  // tiles a warp has in flight before its first wait
   static_assert(GRP <= 8, "one m16n8 tile holds at most 8 heads per kv head");
@@ -244,10 +252,10 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
   // The token sits at position p = len[b] (advanced by the previous step's
   // LM-head kernel, final here); positions < p were written by earlier steps.
   const int p = a.len[b];
-  const int ntile = (p + DTT - 1) / DTT;
+  const int ntile = (p + TT - 1) / TT;
   const int per = (ntile + cs - 1) / cs;
   const int tb = min(ntile, sp * per), te = min(ntile, tb + per);
-  const int nmine = te - tb > warp ? (te - tb - warp + DNW - 1) / DNW : 0;  // tiles tb + warp + DNW * i
+  const int nmine = te - tb > warp ? (te - tb - warp + NW - 1) / NW : 0;  // tiles tb + warp + NW * i
   const uint16_t *Kb = a.kv.base + a.kv.idx(a.layer, 0, b, g, 0);
   const uint16_t *Vb = a.kv.base + a.kv.idx(a.layer, 1, b, g, 0);
   const unsigned ring = (unsigned)__cvta_generic_to_shared(sm) + warp * NS * TL::BYTES;
@@ -256,14 +264,14 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
   // rows past p zero-filled (their scores are masked; zero V keeps P V finite)
   auto issue = [&](int i) {
     if (i < nmine) {
-      const int t0 = (tb + warp + DNW * i) * DTT, n = min(DTT, p - t0);
+      const int t0 = (tb + warp + NW * i) * TT, n = min(TT, p - t0);
       const unsigned st = ring + (i % NS) * TL::BYTES;
 #pragma unroll 4
-      for (int v = lane; v < 2 * DTT * PR; v += 32) {
-        const int kv = v >= DTT * PR, rem = v - kv * DTT * PR, t = rem / PR, c = rem % PR;
+      for (int v = lane; v < 2 * TT * PR; v += 32) {
+        const int kv = v >= TT * PR, rem = v - kv * TT * PR, t = rem / PR, c = rem % PR;
         const bool ok = t < n;
         const uint16_t *src = (kv ? Vb : Kb) + (size_t)(t0 + (ok ? t : 0)) * HD + c * 8;
-        cp16z(st + (kv * DTT + t) * TL::ROW + c * 16, src, ok);
+        cp16z(st + (kv * TT + t) * TL::ROW + c * 16, src, ok);
       }
     }
     cp_commit();
@@ -319,17 +327,18 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
       cp_wait<0>();
       __syncwarp();
     }
-    const unsigned kt = ring + (i % NS) * TL::BYTES, vt = kt + DTT * TL::ROW;
-    const int n = min(DTT, p - (tb + warp + DNW * i) * DTT);
+    const unsigned kt = ring + (i % NS) * TL::BYTES, vt = kt + TT * TL::ROW;
+    const int n = min(TT, p - (tb + warp + NW * i) * TT);
 
-    // S[head][t] for the tile's 32 positions: 4 n-tiles of 8
-    float s[4][4];
+    // S[head][t] for the tile's TT positions: n-tiles of 8
+    constexpr int NT = TT / 8, KK = TT / 16;  // n-tiles of 8 positions, k-steps of 16
+    float s[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
     for (int kp2 = 0; kp2 < KS / 2; ++kp2) {
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
+      for (int nt = 0; nt < NT; ++nt) {
         uint32_t kb[4];  // dims 32 kp2 + 8j of positions 8 nt + 0..7, j = 0..3
         ldsm_x4(kb, kt + (8 * nt + (lane & 7)) * TL::ROW + (32 * kp2 + 8 * (lane >> 3)) * 2);
         mma16816<ACT>(s[nt], qa[2 * kp2], kb);
@@ -339,7 +348,7 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
     // online softmax of head gq over positions 8 nt + 2 tq + {0, 1}
     float mx = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const float v = 8 * nt + 2 * tq + j < n ? s[nt][j] * sl2 : -INFINITY;
@@ -350,10 +359,10 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     const float mnew = fmaxf(mrun, mx);  // finite: the tile has a position < p
     const float corr = exp2f(mrun - mnew);
-    uint32_t ph[2][2], pl[2][2];  // P^T as B fragments: k-step kk = positions 16 kk + ...
+    uint32_t ph[KK][2], pl[KK][2];  // P^T as B fragments: k-step kk = positions 16 kk + ...
     float ls = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
       const float p0 = exp2f(s[nt][0] - mnew), p1 = exp2f(s[nt][1] - mnew);
       ls += p0 + p1;
       const uint32_t hw = pack_act2(p0, p1, ACT);
@@ -379,7 +388,7 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
+      for (int kk = 0; kk < KK; ++kk) {
         uint32_t va[4];  // V^T rows 16 mt + 0..15 x positions 16 kk + 0..15
         ldsm_x4_t(va, vt + (16 * kk + 8 * (lane >> 4) + (lane & 7)) * TL::ROW + (16 * mt + 8 * ((lane >> 3) & 1)) * 2);
         mma16816<ACT>(o[mt], va, ph[kk]);
@@ -395,9 +404,9 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
 
   float *part = reinterpret_cast<float *>(sm);
   float *wpo = part + GRP * HD;
-  float *pm = wpo + DNW * GRP * HD;
+  float *pm = wpo + NW * GRP * HD;
   float *wml = pm + 2 * GRP;
-  float *sps = wml + DNW * GRP * 2;
+  float *sps = wml + NW * GRP * 2;
   float *spv = sps + GRP;
   float *gml = spv + HD;
 #pragma unroll
@@ -417,7 +426,7 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
     wml[(warp * GRP + gq) * 2 + 1] = lrun;
   }
   if (last) {
-    for (int hh = warp; hh < GRP; hh += DNW) {
+    for (int hh = warp; hh < GRP; hh += NW) {
       float d = 0.f;
 #pragma unroll
       for (int r = 0; r < PER; ++r) d = fmaf(qb[hh * HD + lane + 32 * r], kp[r], d);
@@ -432,14 +441,14 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
   __syncthreads();
 
   // the block's state per head: its warps, plus position p in the last split
-  for (int it = tid; it < GRP * HD; it += DNW * 32) {
+  for (int it = tid; it < GRP * HD; it += NW * 32) {
     const int h = it / HD, d = it - h * HD;
     float M = last ? sps[h] : -INFINITY;
 #pragma unroll
-    for (int w = 0; w < DNW; ++w) M = fmaxf(M, wml[(w * GRP + h) * 2]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wml[(w * GRP + h) * 2]);
     float acc = 0.f, Ls = 0.f;
 #pragma unroll
-    for (int w = 0; w < DNW; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const float mw = wml[(w * GRP + h) * 2];
       const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
       acc = fmaf(wt, wpo[(w * GRP + h) * HD + d], acc);
@@ -461,14 +470,14 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
   if (GM) {
     __syncthreads();
     if (cs == 1) {  // the only split: the block's state is the result
-      for (int it = tid; it < GRP * HD; it += DNW * 32)
+      for (int it = tid; it < GRP * HD; it += NW * 32)
         out[it] = round_act(part[it] / pm[2 * (it / HD) + 1], ACT);
       return;
     }
     // publish (O, max, sum) of this split; the last block of (row, kv head)
     // to arrive merges every split's state
     float *gp = a.part + ((size_t)(b * a.Hkv + g) * cs) * GRP * (HD + 2);
-    for (int it = tid; it < GRP * HD; it += DNW * 32) {
+    for (int it = tid; it < GRP * HD; it += NW * 32) {
       const int h = it / HD, d = it - h * HD;
       gp[((size_t)sp * GRP + h) * (HD + 2) + d] = part[it];
     }
@@ -486,10 +495,10 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
     __syncthreads();
     if (!*flag) return;
     __threadfence();
-    for (int it = tid; it < cs * GRP * 2; it += DNW * 32)
+    for (int it = tid; it < cs * GRP * 2; it += NW * 32)
       gml[it] = __ldcg(gp + (size_t)(it >> 1) * (HD + 2) + HD + (it & 1));
     __syncthreads();
-    for (int it = tid; it < GRP * HD; it += DNW * 32) {
+    for (int it = tid; it < GRP * HD; it += NW * 32) {
       const int h = it / HD, d = it - h * HD;
       float M = -INFINITY;
       for (int s2 = 0; s2 < cs; ++s2) M = fmaxf(M, gml[(s2 * GRP + h) * 2]);
@@ -511,7 +520,7 @@ __global__ void __launch_bounds__(DNW * 32, 1) k_attn_dec(AttnArgs a) {
     // shuffles.
     cg::cluster_group cl = cg::this_cluster();
     cl.sync();
-    for (int hh = warp; hh < GRP; hh += DNW) {
+    for (int hh = warp; hh < GRP; hh += NW) {
       const int dpc = HD / cs, r = lane % cs, d0 = sp * dpc + (lane / cs) * 4;
       const bool live = lane < HD / 4;
       float m = -INFINITY, l = 0.f;
@@ -565,17 +574,17 @@ static int device_sms() {
   return n;
 }
 
-template <int HD, int GRP, int ACT, int NS, bool GM>
+template <int HD, int GRP, int ACT, int NW, int TT, int NS, bool GM>
 static cudaError_t launch_dec(const AttnArgs &a, int B, int cs, cudaStream_t s, int pdl) {
-  auto fn = k_attn_dec<HD, GRP, ACT, NS, GM>;
-  size_t smem = dec_smem<HD, NS>(GRP);
+  auto fn = k_attn_dec<HD, GRP, ACT, NW, TT, NS, GM>;
+  size_t smem = dec_smem<HD, NW, TT, NS>(GRP);
   if (!GM && (long)cs * a.Hkv * B <= 2L * device_sms() && smem < kDecSpreadSmem) smem = kDecSpreadSmem;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess && !GM && cs > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, a.Hkv, B);
-  cfg.blockDim = dim3(DNW * 32);
+  cfg.blockDim = dim3(NW * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -640,8 +649,8 @@ int attn_dec_max_cluster(int hd, int grp, int act) {
     cudaError_t e = cudaErrorInvalidValue;
 #define RV_DQ(HD_, G_, A_)                                                                                   \
   if (hd == HD_ && grp == G_ && act == A_) {                                                                 \
-    auto fn = k_attn_dec<HD_, G_, A_, 1, false>;                                                             \
-    cfg.dynamicSmemBytes = dec_smem<HD_, 1>(G_) > kDecSpreadSmem ? dec_smem<HD_, 1>(G_) : kDecSpreadSmem;   \
+    auto fn = k_attn_dec<HD_, G_, A_, DNW, DTT, 1, false>;                                                   \
+    cfg.dynamicSmemBytes = dec_smem<HD_, DNW, DTT, 1>(G_) > kDecSpreadSmem ? dec_smem<HD_, DNW, DTT, 1>(G_) : kDecSpreadSmem; \
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);    \
     if (e == cudaSuccess && cs > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1); \
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);                                  \
@@ -867,12 +876,12 @@ cudaError_t launch_attn_decode(const AttnArgs &a, int B, cudaStream_t s, int pdl
   }
 #define RV_DL(HD_, G_)                                                                                   \
   if (a.hd == HD_ && grp == G_) {                                                                        \
-    constexpr int NSL = DecTile<HD_>::NS_LONG;                                                           \
+    constexpr int NSL = long_slots<HD_>();                                                               \
     if (a.global_merge)                                                                                  \
-      return a.act == 1 ? launch_dec<HD_, G_, 1, NSL, true>(a, B, cs, s, pdl)                            \
-                        : launch_dec<HD_, G_, 0, NSL, true>(a, B, cs, s, pdl);                           \
-    return a.act == 1 ? launch_dec<HD_, G_, 1, 1, false>(a, B, cs, s, pdl)                               \
-                      : launch_dec<HD_, G_, 0, 1, false>(a, B, cs, s, pdl);                              \
+      return a.act == 1 ? launch_dec<HD_, G_, 1, LNW, LTT, NSL, true>(a, B, cs, s, pdl)                  \
+                        : launch_dec<HD_, G_, 0, LNW, LTT, NSL, true>(a, B, cs, s, pdl);                 \
+    return a.act == 1 ? launch_dec<HD_, G_, 1, DNW, DTT, 1, false>(a, B, cs, s, pdl)                     \
+                      : launch_dec<HD_, G_, 0, DNW, DTT, 1, false>(a, B, cs, s, pdl);                    \
   }
   RV_DL(64, 1) RV_DL(64, 2) RV_DL(64, 4) RV_DL(64, 8)
   RV_DL(128, 1) RV_DL(128, 2) RV_DL(128, 4) RV_DL(128, 8)
