@@ -129,6 +129,28 @@ def test_tiny_batched_rows_mixed_paths(weights):
     gm.close()
 
 
+@pytest.mark.parametrize("group", [32, 256])
+def test_tiny_batched_rows_other_groups(weights, group):
+    """Batched river rows on the tensor pipe with group sizes the workloads do
+    not use: 32 (sixteen groups per 512-code chunk) and 256 (one group per
+    chunk of the 256-wide rows; the 688-wide down projection ends in a ragged
+    group).  Forced exits mix both paths in every step; every step is checked
+    layer by layer against the oracle."""
+    B = 3
+    gm, om = pair(weights, B=B, T=32, group=group)
+    ot = layer_oracle(weights, B, 32, group=group)
+    prompts = synth.make_prompt(TINY.vocab, B, 5, seed=8)
+    g_next, g_exit = gm.prefill(prompts, 0.9, fixed_exit=2)
+    o = om.prefill(prompts, 0.9, fixed_exit=2, tf_ids=g_next)
+    assert np.array_equal(o["next_ids"], g_next)
+    toks = list(g_next)
+    for step in range(6):
+        f = np.array([(step + b) % (TINY.n_layers + 1) for b in range(B)], dtype=np.int32)
+        g_next, g_exit = step_both(gm, om, ot, toks, 0.9, f, B)
+        toks = list(g_next)
+    gm.close()
+
+
 def test_tiny_prefill_tau_rule_batched(weights):
     B = 2
     gm, om = pair(weights, B=B, T=24)
