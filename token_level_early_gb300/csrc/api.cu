@@ -405,7 +405,7 @@ int enqueue_layer_rows(rv_model *m, int l, int B, int T, const int32_t *base, cu
   const int32_t *cnt[2] = {m->d_counts, m->d_counts + 1};
   const int act = m->act, d = m->d;
   const int npath = m->has_river ? 2 : 1;
-  RV_CK(cudaMemcpyAsync(m->gHin, m->gH, sizeof(float) * M * d, cudaMemcpyDeviceToDevice, s));
+  RV_CK(launch_copy_rows(m->gH, d, m->gHin, d, d, (int)M, s));  // a kernel, so the layer's launches chain by PDL
   RV_CK(launch_route_lists(m->st.route, B, T, m->gLists, (int)M, m->d_counts, s));
   // attention sub-block
   RV_CK(launch_rmsnorm_rows(m->gH, ly.attn_norm, d, m->c.rms_eps, act, m->gX, nullptr, m->d_nrows, (int)M, s));
@@ -422,7 +422,7 @@ int enqueue_layer_rows(rv_model *m, int l, int B, int T, const int32_t *base, cu
     at.q = m->gQ; at.o = m->gO; at.len = base;
     at.part = m->attn_part; at.counter = m->attn_counter;
     attn_plan(m, B, &at);
-    RV_CK(launch_attn_decode(at, B, s));
+    RV_CK(launch_attn_decode(at, B, s, 1));
   } else {
     AttnRowsArgs ar{};
     ar.kv = m->kv; ar.layer = l; ar.H = m->H; ar.Hkv = m->Hkv; ar.hd = m->hd; ar.act = act;

@@ -14,6 +14,13 @@
 #include "common.cuh"
 #include "kernels.cuh"
 
+// A launch whose error returns from the enclosing launcher.
+#define RV_CK_LAUNCH(call)                     \
+  do {                                         \
+    const cudaError_t e_ = (call);             \
+    if (e_ != cudaSuccess) return e_;          \
+  } while (0)
+
 namespace rv {
 
 static inline int cdiv(long a, long b) { return (int)((a + b - 1) / b); }
@@ -45,6 +52,8 @@ cudaError_t launch_embed(const uint16_t *E, int d, int act, const int32_t *token
 
 // Route state at the start of a step (forced mode: exit 0 = all river).
 __global__ void k_step_init(StepState st, int B, int L) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   if (*st.mode == 1) {
@@ -59,12 +68,14 @@ __global__ void k_step_init(StepState st, int B, int L) {
 }
 
 cudaError_t launch_step_init(const StepState &st, int B, int L, cudaStream_t s) {
-  k_step_init<<<cdiv(B, 128), 128, 0, s>>>(st, B, L);
+  RV_CK_LAUNCH(launch_k(k_step_init, dim3(cdiv(B, 128)), dim3(128), 0, s, 1, st, B, L));
   return cudaGetLastError();
 }
 
 // Index lists of the token rows on each path: lists[p * stride + i].
 __global__ void k_route_lists(const int32_t *route, int B, int T, int32_t *lists, int stride, int32_t *counts) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   extern __shared__ int off[];  // [B]
   if (threadIdx.x == 0) {
     int c0 = 0, c1 = 0;
@@ -85,7 +96,7 @@ __global__ void k_route_lists(const int32_t *route, int B, int T, int32_t *lists
 
 cudaError_t launch_route_lists(const int32_t *route, int B, int T, int32_t *lists, int list_stride,
                                int32_t *counts, cudaStream_t s) {
-  k_route_lists<<<1, 1024, sizeof(int) * B, s>>>(route, B, T, lists, list_stride, counts);
+  RV_CK_LAUNCH(launch_k(k_route_lists, dim3(1), dim3(1024), sizeof(int) * B, s, 1, route, B, T, lists, list_stride, counts));
   return cudaGetLastError();
 }
 
@@ -93,6 +104,8 @@ cudaError_t launch_route_lists(const int32_t *route, int B, int T, int32_t *list
 
 __global__ void k_rmsnorm_rows(const float *H, const uint16_t *gamma, int d, float eps, int act, float *X,
                                const int32_t *list, const int32_t *count) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   __shared__ float red[32];
   for (int idx = blockIdx.x; idx < *count; idx += gridDim.x) {
     const int m = list ? list[idx] : idx;
@@ -110,11 +123,13 @@ __global__ void k_rmsnorm_rows(const float *H, const uint16_t *gamma, int d, flo
 cudaError_t launch_rmsnorm_rows(const float *H, const uint16_t *gamma, int d, float eps, int act, float *X,
                                 const int32_t *list, const int32_t *count, int max_rows, cudaStream_t s) {
   if (max_rows <= 0) return cudaSuccess;
-  k_rmsnorm_rows<<<min(max_rows, 4096), 256, 0, s>>>(H, gamma, d, eps, act, X, list, count);
+  RV_CK_LAUNCH(launch_k(k_rmsnorm_rows, dim3(min(max_rows, 4096)), dim3(256), 0, s, 1, H, gamma, d, eps, act, X, list, count));
   return cudaGetLastError();
 }
 
 __global__ void k_resid_rows(float *H, const float *Y, int d, const int32_t *list, const int32_t *count) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   const long total = (long)(*count) * d;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
     const int idx = (int)(i / d), c = (int)(i % d);
@@ -126,12 +141,14 @@ __global__ void k_resid_rows(float *H, const float *Y, int d, const int32_t *lis
 cudaError_t launch_resid_rows(float *H, const float *Y, int d, const int32_t *list, const int32_t *count,
                               int max_rows, cudaStream_t s) {
   if (max_rows <= 0) return cudaSuccess;
-  k_resid_rows<<<min(cdiv((long)max_rows * d, 256), 8192), 256, 0, s>>>(H, Y, d, list, count);
+  RV_CK_LAUNCH(launch_k(k_resid_rows, dim3(min(cdiv((long)max_rows * d, 256), 8192)), dim3(256), 0, s, 1, H, Y, d, list, count));
   return cudaGetLastError();
 }
 
 // a = round16(silu(gate) * up); Y rows hold [gate (F) | up (F)].
 __global__ void k_swiglu_rows(const float *Y, int F, int act, float *A, const int32_t *list, const int32_t *count) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   const long total = (long)(*count) * F;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
     const int idx = (int)(i / F), c = (int)(i % F);
@@ -144,12 +161,14 @@ __global__ void k_swiglu_rows(const float *Y, int F, int act, float *A, const in
 cudaError_t launch_swiglu_rows(const float *Y, int F, int act, float *A, const int32_t *list,
                                const int32_t *count, int max_rows, cudaStream_t s) {
   if (max_rows <= 0) return cudaSuccess;
-  k_swiglu_rows<<<min(cdiv((long)max_rows * F, 256), 8192), 256, 0, s>>>(Y, F, act, A, list, count);
+  RV_CK_LAUNCH(launch_k(k_swiglu_rows, dim3(min(cdiv((long)max_rows * F, 256), 8192)), dim3(256), 0, s, 1, Y, F, act, A, list, count));
   return cudaGetLastError();
 }
 
 // RoPE on q and k, K/V into the cache slot (layer, sequence, position).
 __global__ void k_rope_rows(RopeRowsArgs a) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   const int half = a.hd / 2, qkv = (a.H + 2 * a.Hkv) * a.hd;
   for (int idx = blockIdx.x; idx < *a.count; idx += gridDim.x) {
     const int m = a.list ? a.list[idx] : idx;
@@ -181,13 +200,15 @@ __global__ void k_rope_rows(RopeRowsArgs a) {
 
 cudaError_t launch_rope_rows(const RopeRowsArgs &a, int max_rows, cudaStream_t s) {
   if (max_rows <= 0) return cudaSuccess;
-  k_rope_rows<<<min(max_rows, 8192), 256, 0, s>>>(a);
+  RV_CK_LAUNCH(launch_k(k_rope_rows, dim3(min(max_rows, 8192)), dim3(256), 0, s, 1, a));
   return cudaGetLastError();
 }
 
 // Token-level decision for each decode row (one block per row).
 __global__ void k_decide_rows(StepState st, const float *Hin, const float *H, int d, int layer1, int L,
                               float *dbg_s) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   __shared__ float red[96];
   const int b = blockIdx.x;
   float dot = 0.f, n1 = 0.f, n2 = 0.f;
@@ -205,7 +226,7 @@ __global__ void k_decide_rows(StepState st, const float *Hin, const float *H, in
 
 cudaError_t launch_decide_rows(const StepState &st, const float *Hin, const float *H, int d, int B, int layer1,
                                int L, float *dbg_s, cudaStream_t s) {
-  k_decide_rows<<<B, 256, 0, s>>>(st, Hin, H, d, layer1, L, dbg_s);
+  RV_CK_LAUNCH(launch_k(k_decide_rows, dim3(B), dim3(256), 0, s, 1, st, Hin, H, d, layer1, L, dbg_s));
   return cudaGetLastError();
 }
 
@@ -227,6 +248,8 @@ __device__ __forceinline__ float ord2f(unsigned o) {
 constexpr int SEQ_TOK_PER_BLOCK = 64;
 
 __global__ void k_seq_smin(StepState st, const float *Hin, const float *H, int d, int T, unsigned *smin) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   __shared__ float wmin[32];
   const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   if (st.route[b] != 0) return;
@@ -256,6 +279,8 @@ __global__ void k_seq_smin(StepState st, const float *Hin, const float *H, int d
 
 __global__ void k_seq_decide(StepState st, int B, int layer1, int L, int fixed_exit, unsigned *smin,
                              float *dbg_smin) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const unsigned o = smin[b];
@@ -281,16 +306,18 @@ __global__ void k_seq_decide(StepState st, int B, int layer1, int L, int fixed_e
 cudaError_t launch_seq_decide(const StepState &st, const float *Hin, const float *H, int d, int B, int T,
                               int layer1, int L, int fixed_exit, unsigned *smin, float *dbg_smin, cudaStream_t s) {
   if (T > 0) {
-    k_seq_smin<<<dim3((T + SEQ_TOK_PER_BLOCK - 1) / SEQ_TOK_PER_BLOCK, B), 256, 0, s>>>(st, Hin, H, d, T, smin);
+    RV_CK_LAUNCH(launch_k(k_seq_smin, dim3(dim3((T + SEQ_TOK_PER_BLOCK - 1) / SEQ_TOK_PER_BLOCK, B)), dim3(256), 0, s, 1, st, Hin, H, d, T, smin));
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  k_seq_decide<<<(B + 127) / 128, 128, 0, s>>>(st, B, layer1, L, fixed_exit, smin, dbg_smin);
+  RV_CK_LAUNCH(launch_k(k_seq_decide, dim3((B + 127) / 128), dim3(128), 0, s, 1, st, B, layer1, L, fixed_exit, smin, dbg_smin));
   return cudaGetLastError();
 }
 
 // Greedy pick per row: largest logit, lowest index on ties.
 __global__ void k_argmax_rows(const float *logits, int V, StepState st, int bump_len, int set_len) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   __shared__ float bv[32];
   __shared__ int bi[32];
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -319,18 +346,20 @@ __global__ void k_argmax_rows(const float *logits, int V, StepState st, int bump
 
 cudaError_t launch_argmax_rows(const float *logits, int V, int B, StepState st, int bump_len, int set_len,
                                cudaStream_t s) {
-  k_argmax_rows<<<B, 1024, 0, s>>>(logits, V, st, bump_len, set_len);
+  RV_CK_LAUNCH(launch_k(k_argmax_rows, dim3(B), dim3(1024), 0, s, 1, logits, V, st, bump_len, set_len));
   return cudaGetLastError();
 }
 
 __global__ void k_copy_rows(const float *src, int src_stride, float *dst, int dst_stride, int d) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   const int b = blockIdx.x;
   for (int i = threadIdx.x; i < d; i += blockDim.x) dst[(size_t)b * dst_stride + i] = src[(size_t)b * src_stride + i];
 }
 
 cudaError_t launch_copy_rows(const float *src, int src_stride, float *dst, int dst_stride, int d, int B,
                              cudaStream_t s) {
-  k_copy_rows<<<B, 256, 0, s>>>(src, src_stride, dst, dst_stride, d);
+  RV_CK_LAUNCH(launch_k(k_copy_rows, dim3(B), dim3(256), 0, s, 1, src, src_stride, dst, dst_stride, d));
   return cudaGetLastError();
 }
 
@@ -343,6 +372,8 @@ constexpr int GBM = 64, GBN = 64, GBK = 16;
 
 __global__ void __launch_bounds__(256) k_gemm_rows(Mat mt, int river, int act, const float *X, float *Y,
                                                    const int32_t *list, const int32_t *count) {
+  pdl_wait();  // griddepcontrol.wait: the previous kernel's results are visible
+  pdl_trigger();
   __shared__ float Xs[GBK][GBM + 4];
   __shared__ float Ws[GBK][GBN + 4];
   __shared__ int rows[GBM];
@@ -426,7 +457,7 @@ cudaError_t launch_gemm_rows(const Mat &m, int river, int act, const float *X, f
   if (max_rows <= 0) return cudaSuccess;
   dim3 grid(cdiv(m.N, GBN), cdiv(max_rows, GBM));
   if (grid.y > 65535) return cudaErrorInvalidValue;
-  k_gemm_rows<<<grid, 256, 0, s>>>(m, river, act, X, Y, list, count);
+  RV_CK_LAUNCH(launch_k(k_gemm_rows, dim3(grid), dim3(256), 0, s, 1, m, river, act, X, Y, list, count));
   return cudaGetLastError();
 }
 

@@ -129,9 +129,6 @@ __global__ void __launch_bounds__(RW * 32, 2) k_rows_mma(Mat mt, const float *X,
   constexpr int GPC = LY::GPC, XR = LY::XR, WR = LY::WR;
   constexpr int WPR = KC / 8;  // words (8 columns) per row and chunk
   extern __shared__ __align__(16) unsigned char sm[];
-  const int cnt = *count;
-  const int r0 = blockIdx.y * RM;
-  if (r0 >= cnt) return;  // the whole cluster shares blockIdx.y
   cg::cluster_group cl = cg::this_cluster();
   const int cs = (int)cl.num_blocks(), rank = (int)cl.block_rank();
   const int n0 = blockIdx.x * RN;
@@ -143,6 +140,48 @@ __global__ void __launch_bounds__(RW * 32, 2) k_rows_mma(Mat mt, const float *X,
   int *rows = reinterpret_cast<int *>(sm + LY::ROWS);
   float *xg = reinterpret_cast<float *>(sm + LY::XG);
   const __half2 *wsz = reinterpret_cast<const __half2 *>(sm + LY::SZ);
+
+  // the warp's 16 weight rows of chunk kc (and their (scale, zero) words)
+  auto stage_w = [&](int kc) {
+    const int k0 = kc * KC;
+    const unsigned wdst = sbase + LY::WS + warp * 16 * WR;
+    constexpr int PPR = (I4 ? KC / 2 : KC * 2) / 16;  // 16-byte pieces per row
+    for (int p = lane; p < 16 * PPR; p += 32) {
+      const int r = p / PPR, c = p % PPR, n = n0 + warp * 16 + r;
+      bool ok;
+      const void *src;
+      if (I4) {
+        ok = n < N && k0 + 32 * c < R.Kp;
+        src = R.q + (ok ? (size_t)n * (R.Kp >> 3) + (k0 >> 3) + 4 * c : 0);
+      } else {
+        ok = n < N && k0 + 8 * c < K;
+        src = mt.w + (ok ? (size_t)n * K + k0 + 8 * c : 0);
+      }
+      cp16_or_zero(wdst + r * WR + 16 * c, src, ok);
+    }
+    if (I4) {
+      const unsigned sdst = sbase + LY::SZ + warp * 16 * GPC * 4;
+      for (int p = lane; p < 16 * GPC; p += 32) {
+        const int r = p / (GPC ? GPC : 1), j = p % (GPC ? GPC : 1), n = n0 + warp * 16 + r;
+        const int gi = k0 / (GS ? GS : 1) + j;
+        const bool ok = n < N && gi < R.G;
+        cp4_or_zero(sdst + p * 4, R.sz + (ok ? (size_t)n * R.Gs + gi : 0), ok);
+      }
+    }
+    cp_commit();
+  };
+  const int nkc = (Kw + KC - 1) / KC;
+  // the weights do not depend on the previous kernel: the first chunk's copies
+  // are issued before the programmatic-dependent-launch wait
+  if (rank < nkc) stage_w(rank);
+  pdl_wait();
+  pdl_trigger();
+  const int cnt = *count;
+  const int r0 = blockIdx.y * RM;
+  if (r0 >= cnt) {  // the whole cluster shares blockIdx.y
+    cp_wait<0>();
+    return;
+  }
   if (tid < RM) rows[tid] = r0 + tid < cnt ? (list ? list[r0 + tid] : r0 + tid) : -1;
   __syncthreads();
 
@@ -157,37 +196,9 @@ __global__ void __launch_bounds__(RW * 32, 2) k_rows_mma(Mat mt, const float *X,
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
-  const int nkc = (Kw + KC - 1) / KC;
   for (int kc = rank; kc < nkc; kc += cs) {
     const int k0 = kc * KC;
-    // the warp's 16 weight rows (and their (scale, zero) words)
-    {
-      const unsigned wdst = sbase + LY::WS + warp * 16 * WR;
-      constexpr int PPR = (I4 ? KC / 2 : KC * 2) / 16;  // 16-byte pieces per row
-      for (int p = lane; p < 16 * PPR; p += 32) {
-        const int r = p / PPR, c = p % PPR, n = n0 + warp * 16 + r;
-        bool ok;
-        const void *src;
-        if (I4) {
-          ok = n < N && k0 + 32 * c < R.Kp;
-          src = R.q + (ok ? (size_t)n * (R.Kp >> 3) + (k0 >> 3) + 4 * c : 0);
-        } else {
-          ok = n < N && k0 + 8 * c < K;
-          src = mt.w + (ok ? (size_t)n * K + k0 + 8 * c : 0);
-        }
-        cp16_or_zero(wdst + r * WR + 16 * c, src, ok);
-      }
-      if (I4) {
-        const unsigned sdst = sbase + LY::SZ + warp * 16 * GPC * 4;
-        for (int p = lane; p < 16 * GPC; p += 32) {
-          const int r = p / (GPC ? GPC : 1), j = p % (GPC ? GPC : 1), n = n0 + warp * 16 + r;
-          const int gi = k0 / (GS ? GS : 1) + j;
-          const bool ok = n < N && gi < R.G;
-          cp4_or_zero(sdst + p * 4, R.sz + (ok ? (size_t)n * R.Gs + gi : 0), ok);
-        }
-      }
-      cp_commit();
-    }
+    if (kc != rank) stage_w(kc);
     // X chunk as 16-bit pairs: int4 weights (x[8w + t], x[8w + t + 4]) with
     // per-group sums, 16-bit weights (x[8w + 2t], x[8w + 2t + 1]); thread:
     // word w of rows i0, i0 + RPP, ..., four rows' loads in flight before any
@@ -360,13 +371,15 @@ cudaError_t launch_kc(const Mat &m, const float *X, float *Y, const int32_t *lis
   cfg.blockDim = dim3(RW * 32);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = cs;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // the kernel waits with griddepcontrol
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, fn, m, X, Y, list, count, amax);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -417,6 +430,8 @@ cudaError_t launch_rows_b16(const Mat &m, int act, const float *X, float *Y, con
 // 0..B-1), which are zeroed again for the next step; the length update of
 // k_argmax_rows.
 __global__ void k_pick_finish(unsigned long long *amax, int B, StepState st, int bump_len, int set_len) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const unsigned long long key = amax[b];
@@ -428,8 +443,7 @@ __global__ void k_pick_finish(unsigned long long *amax, int B, StepState st, int
 
 cudaError_t launch_pick_finish(unsigned long long *amax, int B, StepState st, int bump_len, int set_len,
                                cudaStream_t s) {
-  k_pick_finish<<<(B + 127) / 128, 128, 0, s>>>(amax, B, st, bump_len, set_len);
-  return cudaGetLastError();
+  return launch_k(k_pick_finish, dim3((B + 127) / 128), dim3(128), 0, s, 1, amax, B, st, bump_len, set_len);
 }
 
 }  // namespace rv
