@@ -262,6 +262,55 @@ __global__ void __launch_bounds__(RW * 32, 2) k_rows_mma(Mat mt, const float *X,
       const unsigned char *wr1 = wr0 + 8 * WR;
 #pragma unroll 1
       for (int j = 0; j < GPC; ++j) {
+        if constexpr (GS > 0 && GS <= 128) {
+          // the group's A fragments (unpacked once), then the listed rows as
+          // two halves of 4 n8-tiles: 16 registers of D instead of 32 under
+          // the register budget of two blocks per SM (each tile's MMAs in the
+          // same order as below; groups of 256 keep the one-pass form, whose
+          // A fragments would not fit)
+          uint32_t A[GS / 32 > 0 ? GS / 32 : 1][8];
+#pragma unroll
+          for (int s2 = 0; s2 < GS / 32; ++s2) {
+            const int wd = (j * GS + 32 * s2) / 8;
+            const uint4 u0 = *reinterpret_cast<const uint4 *>(wr0 + 4 * wd);
+            const uint4 u1 = *reinterpret_cast<const uint4 *>(wr1 + 4 * wd);
+            A[s2][0] = code_pair(u0.x, rot, cmask, cbits); A[s2][1] = code_pair(u1.x, rot, cmask, cbits);
+            A[s2][2] = code_pair(u0.y, rot, cmask, cbits); A[s2][3] = code_pair(u1.y, rot, cmask, cbits);
+            A[s2][4] = code_pair(u0.z, rot, cmask, cbits); A[s2][5] = code_pair(u1.z, rot, cmask, cbits);
+            A[s2][6] = code_pair(u0.w, rot, cmask, cbits); A[s2][7] = code_pair(u1.w, rot, cmask, cbits);
+          }
+          const float2 z0 = __half22float2(wsz[(warp * 16 + gq) * GPC + j]);
+          const float2 z1 = __half22float2(wsz[(warp * 16 + gq + 8) * GPC + j]);
+          const float c0 = -(16.f + z0.y), c1 = -(16.f + z1.y);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            float D[4][4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) D[t][0] = D[t][1] = D[t][2] = D[t][3] = 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < GS / 32; ++s2) {
+              const int wd = (j * GS + 32 * s2) / 8;
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int nt = 4 * hf + t;
+                uint32_t b[4];  // words wd .. wd + 3 of rows 8 nt .. 8 nt + 7
+                ldsm4(b, sbase + LY::XS + (8 * nt + (lane & 7)) * XR + (wd + (lane >> 3)) * 16);
+                mma_16816<ACT>(D[t], A[s2], b);
+                mma_16816<ACT>(D[t], A[s2] + 4, b + 2);
+              }
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int nt = 4 * hf + t;
+              const float X0 = xg[(8 * nt + 2 * tq) * GPC + j], X1 = xg[(8 * nt + 2 * tq + 1) * GPC + j];
+              acc[nt][0] = fmaf(z0.x, fmaf(c0, X0, 16.f * D[t][0]), acc[nt][0]);
+              acc[nt][1] = fmaf(z0.x, fmaf(c0, X1, 16.f * D[t][1]), acc[nt][1]);
+              acc[nt][2] = fmaf(z1.x, fmaf(c1, X0, 16.f * D[t][2]), acc[nt][2]);
+              acc[nt][3] = fmaf(z1.x, fmaf(c1, X1, 16.f * D[t][3]), acc[nt][3]);
+            }
+          }
+          continue;
+        }
         float D[8][4];
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) D[nt][0] = D[nt][1] = D[nt][2] = D[nt][3] = 0.f;
