@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(RW * 32, 2) k_rows_mma(Mat mt, const float *X,
     // is converted
     {
       constexpr int RPP = RW * 32 / WPR;  // rows per pass
-      constexpr int NB = 4;               // rows per batch of loads
+      constexpr int NB = I4 ? 4 : 8;      // rows per batch of loads
       static_assert((RM / RPP) % NB == 0, "whole batches of rows");
       const int w = tid % WPR, i0 = tid / WPR, k = k0 + 8 * w;
       const bool full = k + 8 <= K;
