@@ -207,6 +207,26 @@ int rv_debug_fail_alloc(int after);
 #define RV_TIME_ATTN 3
 int rv_time_kernel(rv_model *m, int kind, int layer, int river, int iters, float *ms_per_launch, double *bytes);
 
+/* Launch plan of the decode attention (host arithmetic only, no device
+ * work; the pages have no counterpart: the plan is how this library splits
+ * the attention over a single token's K/V, the "Memory Efficiency" long
+ * contexts of paperlayer.ai section 5 included).  For `batch` rows with
+ * n_kv_heads KV heads each, on a GPU of n_sm SMs whose largest launchable
+ * cluster is max_cluster (a power of two <= 16), the longest context being
+ * `context` positions: returns 0 for the cluster plan (the splits of a
+ * (row, KV head) form one thread-block cluster and merge through
+ * distributed shared memory; *splits = the cluster size: the largest power
+ * of two <= max_cluster with splits x n_kv_heads x batch <= 2 n_sm) when
+ * each warp of a split has at most 4 tiles of 32 positions, or when the
+ * rows alone fill the GPU (n_sm / (n_kv_heads x batch) < 2); else 1 for the
+ * global-merge plan (*splits = min(n_sm / (n_kv_heads x batch),
+ * max_splits, 128) blocks per (row, KV head), merged through global
+ * memory).  The decode step keys its captured graph by this plan.
+ * RV_EINVAL for a null splits, batch, n_kv_heads, n_sm or max_splits below
+ * 1, a negative context, or max_cluster not a power of two in 1..16. */
+int rv_decode_attention_plan(int batch, int n_kv_heads, int n_sm, int max_cluster, int max_splits, int context,
+                             int *splits);
+
 /* Greedy LM head without allocation: final RMSNorm (gain d_final_norm, eps
  * rms_eps) of the fp32 vector d_h [d_model], the LM-head GEMV against
  * d_lm_head [vocab][d_model] (16-bit, act_dtype 0 = fp16, 1 = bf16) and the

@@ -29,7 +29,7 @@ DUMP_HIDDEN, DUMP_S, DUMP_LOGITS, DUMP_KV, DUMP_LENS = range(5)
 EXPORTED = ("rv_last_error", "rv_load_model", "rv_quantize_river", "rv_export_river", "rv_prefill",
             "rv_decode_step", "rv_decode_step_dev", "rv_sync_status", "rv_kv_reset", "rv_set_debug",
             "rv_debug_dump", "rv_kv_bytes", "rv_param_bytes", "rv_free_model", "rv_time_kernel", "rv_greedy_head_noalloc", "rv_offload_backbone",
-            "rv_set_option", "rv_debug_fail_alloc")
+            "rv_set_option", "rv_debug_fail_alloc", "rv_decode_attention_plan")
 OPT_DECODE_ENGINE, ENGINE_CHAIN, ENGINE_PERSISTENT = 0, 0, 1
 OPT_QUANTIZER, QUANT_RTN, QUANT_HQQ = 1, 0, 1
 OPT_WAIT_LIMIT_US = 2
@@ -124,6 +124,7 @@ def lib():
         "rv_greedy_head_noalloc": ([vp, vp, vp, i32, i32, i32, f32, vp, vp, vp], i32),
         "rv_set_option": ([vp, i32, i32], i32),
         "rv_debug_fail_alloc": ([i32], i32),
+        "rv_decode_attention_plan": ([i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -147,6 +148,17 @@ def greedy_head_noalloc(d_lm_head: int, d_final_norm: int, d_h: int, vocab: int,
     """rv_greedy_head_noalloc on device pointers (see include/rv.h)."""
     _check(lib().rv_greedy_head_noalloc(d_lm_head, d_final_norm, d_h, vocab, d_model, act_dtype, float(rms_eps),
                                         d_next_id, d_logits, stream))
+
+
+def decode_attention_plan(batch: int, n_kv_heads: int, n_sm: int, max_cluster: int, max_splits: int,
+                          context: int):
+    """rv_decode_attention_plan (host arithmetic, no GPU needed): returns
+    (plan, splits), plan 0 = cluster plan, 1 = global-merge plan."""
+    sp = ctypes.c_int(0)
+    rc = lib().rv_decode_attention_plan(batch, n_kv_heads, n_sm, max_cluster, max_splits, context, ctypes.byref(sp))
+    if rc < 0:
+        _check(rc)
+    return rc, sp.value
 
 
 def debug_fail_alloc(after: int) -> None:

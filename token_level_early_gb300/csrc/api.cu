@@ -1210,6 +1210,17 @@ int rv_debug_fail_alloc(int after) {
   return RV_OK;
 }
 
+int rv_decode_attention_plan(int batch, int n_kv_heads, int n_sm, int max_cluster, int max_splits, int context,
+                             int *splits) {
+  g_err.clear();
+  if (!splits) return fail(RV_EINVAL, "null pointer");
+  if (batch < 1 || n_kv_heads < 1 || n_sm < 1 || max_splits < 1 || context < 0)
+    return fail(RV_EINVAL, "bad argument");
+  if (max_cluster < 1 || max_cluster > 16 || (max_cluster & (max_cluster - 1)))
+    return fail(RV_EINVAL, "max_cluster must be a power of two <= 16");
+  return attn_dec_plan(batch, n_kv_heads, n_sm, max_cluster, max_splits, context, splits);
+}
+
 int rv_offload_backbone(rv_model *m, int keep_layers) {
   g_err.clear();
   if (check_common(m)) return RV_EINVAL;
